@@ -1,0 +1,514 @@
+"""Benchmark: MLA ragged prefill TFLOP/s on GB300 (one JSON line on stdout).
+
+Default workload: 8 ragged causal requests, lengths uniform in [512, 4096]
+(seeded), 128 heads, Q/K dim 192, V dim 128, bf16 -- the DeepSeek-R1-shaped
+prefill the metric is quoted on.  A step is one pass of the hot path over
+that batch: the work list comes from the plan (made once per batch, reused
+by every layer) and the step is one ``mla_prefill_run``.  The chunked-prefix
+path (gather -> up-projection -> non-causal chunk attention -> merge) is
+timed on the 4 x (2048 new + 8192 cached) workload and reported under
+``chunked_prefix``.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the
+same workload (there is no runnable reference implementation).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from chunked_prefill_attention_ragged_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "MLA ragged prefill TFLOP/s (Dqk192/Dv128, bf16) and % of GB300 BF16 TC peak"
+FLOP_PER_PAIR = 2 * (wl.DQK + wl.DV)      # QK^T (2*192) + PV (2*128) per allowed (query, key) pair and head
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------------------- accounting
+def allowed_pairs(q_lens, kv_lens, causal: bool) -> int:
+    """Allowed (query, key) pairs of one head, counted exactly (bottom-right causal)."""
+    total = 0
+    for lq, lkv in zip(q_lens, kv_lens):
+        lq, lkv = int(lq), int(lkv)
+        if not causal:
+            total += lq * lkv
+            continue
+        d = lkv - lq
+        # row i sees keys 0..i+d clipped to [0, lkv)
+        for_rows = np.clip(np.arange(lq) + d + 1, 0, lkv)
+        total += int(for_rows.sum())
+    return total
+
+
+def attention_flops(q_lens, kv_lens, heads: int, causal: bool) -> float:
+    return float(allowed_pairs(q_lens, kv_lens, causal)) * heads * FLOP_PER_PAIR
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    out = {"bf16_tflops": FALLBACK_BF16_TFLOPS, "bf16_tflops_sustained": None, "hbm_gbs": FALLBACK_HBM_GBS,
+           "source": "fallback"}
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+
+            def find(keys):
+                for k in keys:
+                    if k in d and isinstance(d[k], (int, float)):
+                        return float(d[k])
+                return None
+            bf = find(["bf16_tflops", "bf16_tflops_burst"])
+            bs = find(["bf16_tflops_sustained"])
+            hb = find(["hbm_gbs", "hbm_GBs", "hbm_gb_s"])
+            if bf:
+                out["bf16_tflops"] = bf
+                out["source"] = "measured"
+            if bs:
+                out["bf16_tflops_sustained"] = bs
+            if hb:
+                out["hbm_gbs"] = hb
+        except Exception:
+            pass
+    return out
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("attn_kernel.cu", "ptx.cuh", "tmem_wide.cuh", "planner.cpp", "planner.h"):
+        with open(os.path.join(ROOT, "chunked_prefill_attention_ragged_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic():
+    """DRAM bytes per launch of the attention kernel from the committed ncu summary, if it
+    was taken on the current kernel source; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "prefill_attention_traffic.json")
+    try:
+        d = json.load(open(path))
+        if d.get("kernel_source_hash") == kernel_source_hash():
+            return d.get("dram_bytes_per_launch_full_workload")
+    except Exception:
+        pass
+    return None
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.25)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, p in zip(names, parts[2:6]):
+                if p.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+def _oracle_job(args):
+    """One (request, head) of the oracle; run in a spawned single-threaded worker."""
+    q, k, v, sm_scale = args
+    from oracle import attend_request
+    t0 = time.perf_counter()
+    attend_request(q, k, v, causal=True, sm_scale=sm_scale)
+    return time.perf_counter() - t0
+
+
+def time_oracle_sample(batch: wl.RaggedBatch, target_s: float = 15.0, max_workers: int | None = None):
+    """Time the fp64 oracle on (request, head) pieces of the workload until about
+    target_s of wall time is spent; returns (TFLOP/s, cores, sample description)."""
+    import multiprocessing as mp
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"        # inherited by spawned workers: one BLAS thread each
+    workers = max_workers or os.cpu_count() or 1
+    qo, kv = batch.qo_indptr, batch.kv_indptr
+    # Shortest request first so the sample finishes in bounded time.
+    order = np.argsort(batch.q_lens)
+    r = int(order[0])
+    L = int(batch.q_lens[r])
+    jobs = []
+    for h in range(batch.num_heads):
+        jobs.append((batch.q[qo[r]:qo[r + 1], h:h + 1], batch.k[kv[r]:kv[r + 1], h:h + 1],
+                     batch.v[kv[r]:kv[r + 1], h:h + 1], batch.sm_scale))
+    ctx = mp.get_context("spawn")
+    done_heads = 0
+    t0 = time.perf_counter()
+    with ctx.Pool(workers) as pool:
+        for start in range(0, len(jobs), workers):
+            pool.map(_oracle_job, jobs[start:start + workers])
+            done_heads += len(jobs[start:start + workers])
+            if time.perf_counter() - t0 > target_s:
+                break
+    wall = time.perf_counter() - t0
+    flops = attention_flops([L], [L], done_heads, True)
+    return flops / wall / 1e12, workers, (f"request {r} (L={L}) x {done_heads} of {batch.num_heads} heads, "
+                                          f"{workers} spawned single-thread fp64 numpy workers, {wall:.1f} s")
+
+
+# ----------------------------------------------------------------------------- our arm
+def bench_ours(args, world, rank, local):
+    import torch
+    import chunked_prefill_attention_ragged_gb300 as mla
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    peaks = load_peaks()
+    b = wl.make_workload(args.workload)
+    flops = attention_flops(b.q_lens, b.kv_lens, b.num_heads, b.causal)
+
+    # CPU baseline first (spawned pool, before the GPU is busy), rank 0 at N=1 only.
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, sample = time_oracle_sample(b, target_s=args.cpu_seconds)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample}
+
+    def dev_bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    q, k, v = dev_bf16(b.q), dev_bf16(b.k), dev_bf16(b.v)
+    stream = torch.cuda.current_stream(dev)
+    plan = mla.mla_prefill_plan(b.qo_indptr, b.kv_indptr, b.num_heads, causal=b.causal, sm_scale=b.sm_scale,
+                                window_left=b.window_left, logits_soft_cap=b.logits_soft_cap)
+    o = torch.empty((b.q.shape[0], b.num_heads, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((b.q.shape[0], b.num_heads), dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        plan.run(q, k, v, o, lse)
+    torch.cuda.synchronize()
+    plan.status()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # ---- device-timed region: K steps, inputs resident (2.4 GB >> 129 MB L2)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            plan.run(q, k, v, o, lse)
+            ev[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    plan.status()
+    total_ms = t_start.elapsed_time(t_end)
+    launch_ms = [a.elapsed_time(c) for a, c in ev]
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = flops * world / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end to end through the public API with host buffers
+    pin = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).pin_memory()  # noqa: E731
+    hq, hk, hv = pin(b.q), pin(b.k), pin(b.v)
+    ho = torch.empty(o.shape, dtype=torch.int16).pin_memory()
+    hl = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    dq, dk, dv = (torch.empty(x.shape, dtype=torch.int16, device=dev) for x in (hq, hk, hv))
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        p = mla.mla_prefill_plan(b.qo_indptr, b.kv_indptr, b.num_heads, causal=b.causal, sm_scale=b.sm_scale,
+                                 window_left=b.window_left, logits_soft_cap=b.logits_soft_cap)
+        p.run(dq.view(torch.bfloat16), dk.view(torch.bfloat16), dv.view(torch.bfloat16), o, lse)
+        ho.copy_(o.view(torch.int16), non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+        return p
+    keep = [e2e_step() for _ in range(2)]
+    torch.cuda.synchronize()
+    e_steps = max(1, min(args.steps, 5))
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e_steps):
+        keep.append(e2e_step())
+    torch.cuda.synchronize()
+    barrier()
+    e2e_s = (time.perf_counter() - t0) / e_steps
+    del keep
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
+    d2h = ho.numel() * 2 + hl.numel() * 4
+
+    # ---- chunked-prefix path rows (workload 2), rank 0
+    chunked = None
+    if rank == 0 and not args.no_chunked:
+        chunked = bench_chunked(args, dev, peaks)
+
+    if rank != 0:
+        return None
+    avg_launch_ms = sum(launch_ms) / len(launch_ms)
+    achieved = flops / (avg_launch_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16; no dataset)",
+        "config": {
+            "workload": wl.WORKLOAD_NAMES[args.workload],
+            "requests": int(b.batch),
+            "q_lens": [int(x) for x in b.q_lens],
+            "heads": b.num_heads, "head_dim_qk": 192, "head_dim_vo": 128, "causal": b.causal,
+            "sm_scale": b.sm_scale, "window_left": b.window_left, "logits_soft_cap": b.logits_soft_cap,
+            "flop_per_step": flops, "allowed_pairs_per_head": allowed_pairs(b.q_lens, b.kv_lens, b.causal),
+            "l2": "no flush: inputs (%.2f GB) far larger than the 129 MB L2" % ((q.numel() + k.numel() + v.numel()) * 2 / 1e9),
+            "parallelism": f"replicas x{world} (each rank runs its own batch)",
+        },
+        "pct_of_bf16_peak": round(100.0 * value / world / peaks["bf16_tflops"], 2),
+        "roofline": {
+            "kernel": "prefill_kernel",
+            "bound": "tensor",
+            "achieved": round(achieved, 2),
+            "peak": peaks["bf16_tflops"],
+            "peak_source": f"{peaks['source']} bf16 dense (burst)",
+            "unit": "TFLOP/s",
+            "frac": round(achieved / peaks["bf16_tflops"], 4),
+            "traffic": committed_traffic(),
+            "avg_launch_ms": round(avg_launch_ms, 4),
+        },
+        "e2e": {"value": round(flops / e2e_s / 1e12, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 3),
+                "includes": "pinned H2D of Q/K/V, plan, run, D2H of O/LSE"},
+        "cpu_baseline": cpu,
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "plan_units": plan.num_units, "plan_ctas": plan.num_ctas,
+    }
+    if chunked is not None:
+        line["chunked_prefix"] = chunked
+    return line
+
+
+def bench_chunked(args, dev, peaks):
+    """Per-row timings of the chunked-prefix pipeline on workload 2 (4 x (2048 + 8192 cached))."""
+    import torch
+    import chunked_prefill_attention_ragged_gb300 as mla
+    from chunked_prefill_attention_ragged_gb300.pipeline import ChunkedPrefill
+
+    cb = wl.make_chunked_prefix()
+    b = cb.new
+
+    def dev_bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    q, k, v = dev_bf16(b.q), dev_bf16(b.k), dev_bf16(b.v)
+    cache, w = dev_bf16(cb.cache), dev_bf16(cb.w_kvb)
+    table = torch.from_numpy(cb.block_table).to(dev)
+    pipe = ChunkedPrefill(b.qo_indptr, cb.layout.cu_seq_lens, cb.layout.chunk_starts, b.num_heads,
+                          sm_scale=b.sm_scale, device=dev)
+    o = torch.empty((b.q.shape[0], b.num_heads, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((b.q.shape[0], b.num_heads), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(2):
+        pipe.run(q, k, v, cache, table, w, o, lse)
+    torch.cuda.synchronize()
+    pipe.check_status()
+    stream = torch.cuda.current_stream(dev)
+    reps = 5
+    names = ["main_attention", "gather", "up_proj", "chunk_attention", "merge"]
+    acc = {n: [] for n in names}
+    total = []
+    nC = pipe.cu.shape[0]
+    for _ in range(reps):
+        flush.zero_()
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 + 8 * nC)]
+        i = 0
+        evs[i].record(stream); i += 1
+        pipe.main.run(q, k, v, o, lse)
+        evs[i].record(stream); i += 1
+        marks = []
+        for c, plan in enumerate(pipe.chunks):
+            t = pipe.chunk_tokens[c]
+            lat, kc, vc = pipe.latent[:t], pipe.k_c[:t], pipe.v_c[:t]
+            e0 = evs[i]; e0.record(stream); i += 1
+            mla.mla_gather_latent(cache, table, pipe.cu_dev[c], pipe.starts_dev[c], t, lat, pipe.status)
+            e1 = evs[i]; e1.record(stream); i += 1
+            mla.mla_up_proj(lat, w, b.num_heads, kc, vc, pipe.status)
+            e2 = evs[i]; e2.record(stream); i += 1
+            plan.run(q, kc, vc, pipe.o_c, pipe.lse_c)
+            e3 = evs[i]; e3.record(stream); i += 1
+            mla.mla_merge_state(o, lse, pipe.o_c, pipe.lse_c, o, lse)
+            e4 = evs[i]; e4.record(stream); i += 1
+            marks.append((e0, e1, e2, e3, e4))
+        torch.cuda.synchronize()
+        acc["main_attention"].append(evs[0].elapsed_time(evs[1]))
+        for e0, e1, e2, e3, e4 in marks:
+            acc["gather"].append(e0.elapsed_time(e1))
+            acc["up_proj"].append(e1.elapsed_time(e2))
+            acc["chunk_attention"].append(e2.elapsed_time(e3))
+            acc["merge"].append(e3.elapsed_time(e4))
+        total.append(evs[0].elapsed_time(marks[-1][4]))
+    pipe.check_status()
+    med = {n: statistics.median(x) for n, x in acc.items()}
+    T = int(pipe.chunk_tokens[0])
+    rows = b.q.shape[0]
+    gather_bytes = 2 * T * 576 * 2
+    merge_bytes = rows * b.num_heads * (3 * 128 * 2 + 3 * 4)
+    upf = 2.0 * T * 512 * b.num_heads * 256
+    up_bytes = T * 576 * 2 + 512 * b.num_heads * 256 * 2 + T * b.num_heads * (192 + 128) * 2
+    main_f = attention_flops(b.q_lens, b.q_lens, b.num_heads, True)
+    chunk_f = attention_flops(b.q_lens, np.diff(pipe.cu[0]), b.num_heads, False)
+    total_f = main_f + nC * (chunk_f + upf)
+    hbm = peaks["hbm_gbs"]
+    return {
+        "workload": wl.WORKLOAD_NAMES[2],
+        "chunks": nC, "chunk_tokens_per_request": cb.chunk_tokens,
+        "l2": "256 MB buffer written before each repetition",
+        "step_ms": round(statistics.median(total), 4),
+        "step_tflops": round(total_f / (statistics.median(total) * 1e-3) / 1e12, 2),
+        "main_attention": {"ms": round(med["main_attention"], 4),
+                           "tflops": round(main_f / med["main_attention"] / 1e9, 2)},
+        "chunk_attention": {"ms": round(med["chunk_attention"], 4),
+                            "tflops": round(chunk_f / med["chunk_attention"] / 1e9, 2)},
+        "up_proj": {"ms": round(med["up_proj"], 4), "tflops": round(upf / med["up_proj"] / 1e9, 2),
+                    "gbs": round(up_bytes / med["up_proj"] / 1e6, 1)},
+        "gather": {"ms": round(med["gather"], 4), "gbs": round(gather_bytes / med["gather"] / 1e6, 1),
+                   "frac_hbm": round(gather_bytes / med["gather"] / 1e6 / hbm, 3)},
+        "merge": {"ms": round(med["merge"], 4), "gbs": round(merge_bytes / med["merge"] / 1e6, 1),
+                  "frac_hbm": round(merge_bytes / med["merge"] / 1e6 / hbm, 3)},
+        "hbm_peak_gbs": hbm, "hbm_peak_source": peaks["source"],
+    }
+
+
+# ----------------------------------------------------------------------------- reference arm
+def bench_reference(args, world, rank):
+    if rank != 0:
+        return None
+    b = wl.make_workload(args.workload)
+    per_step = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        time_oracle_sample(b, target_s=per_step)
+    vals, desc, cores = [], "", 1
+    for _ in range(args.steps):
+        v, cores, desc = time_oracle_sample(b, target_s=per_step)
+        vals.append(v)
+    value = statistics.median(vals)
+    flops = attention_flops(b.q_lens, b.kv_lens, b.num_heads, b.causal)
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(flops / (value * 1e12) * 1e3, 1) if value > 0 else None,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16; no dataset)",
+        "config": {"workload": wl.WORKLOAD_NAMES[args.workload], "heads": b.num_heads,
+                   "q_lens": [int(x) for x in b.q_lens]},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "note": "the pages publish no runnable implementation; the reference arm is the fp64 oracle on host cores",
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=1, choices=[0, 1, 3, 4])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-chunked", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        line = bench_reference(args, world, rank)
+    else:
+        line = bench_ours(args, world, rank, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,265 @@
+"""ctypes binding over libmla_prefill.so (argument marshalling only).
+
+Every function mirrors one C entry point of ``include/mla_prefill.h`` under
+the same name.  Tensors are torch tensors: device memory and the current
+CUDA stream come from torch, all arithmetic happens in the library's
+kernels.  There is no fallback: if the shared library cannot be built or
+loaded, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+import numpy as np
+
+from . import _build
+
+_lib = None
+_lock = threading.Lock()
+
+MLA_OK = 0
+_c_int, _c_i64, _c_f, _c_vp = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_i64p = ctypes.POINTER(ctypes.c_int64)
+
+_SIGNATURES = {
+    "mla_error_string": (ctypes.c_char_p, [_c_int]),
+    "mla_abi_version": (_c_int, []),
+    "mla_prefill_plan": (_c_int, [ctypes.POINTER(_c_vp), _i32p, _i32p, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                  _c_f, _c_int, _c_f, _c_vp]),
+    "mla_prefill_run": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
+    "mla_prefill_status": (_c_int, [_c_vp]),
+    "mla_plan_destroy": (_c_int, [_c_vp]),
+    "mla_plan_query": (_c_int, [_c_vp, _c_int, _i64p]),
+    "mla_plan_units_host": (_c_int, [_i32p, _i32p, _c_int, _c_int, _c_int, _c_int, _c_int, _i32p, _c_i64, _i32p,
+                                     _i64p]),
+    "mla_gather_latent": (_c_int, [_c_vp, _c_i64, _c_int, _c_int, _c_vp, _c_int, _c_vp, _c_vp, _c_int, _c_i64,
+                                   _c_vp, _c_vp, _c_vp]),
+    "mla_up_proj": (_c_int, [_c_vp, _c_vp, _c_i64, _c_int, _c_vp, _c_vp, _c_vp, _c_vp]),
+    "mla_merge_state": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_int, _c_int, _c_vp]),
+}
+EXPORTED = tuple(_SIGNATURES)
+
+
+class MlaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {error_string(code)} ({code})")
+
+
+def library(build_if_stale: bool = True) -> ctypes.CDLL:
+    """Load (building first if needed) the shared library."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build() if build_if_stale else _build.LIB_PATH
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def error_string(code: int) -> str:
+    return library().mla_error_string(code).decode()
+
+
+def _check(code: int, what: str):
+    if code != MLA_OK:
+        raise MlaError(code, what)
+
+
+def _host_i32(x) -> np.ndarray:
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int32))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(_i32p)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dev(t, dtype, name):
+    import torch
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+# ---------------------------------------------------------------------------- plan
+class PrefillPlan:
+    """Owns an ``mla_plan_t``; created by :func:`mla_prefill_plan`."""
+
+    def __init__(self, handle: ctypes.c_void_p, num_heads: int, total_q: int, total_kv: int):
+        self._h = handle
+        self.num_heads = num_heads
+        self.total_q = total_q
+        self.total_kv = total_kv
+
+    @property
+    def handle(self):
+        return self._h
+
+    def query(self, which: int) -> int:
+        v = ctypes.c_int64(0)
+        _check(library().mla_plan_query(self._h, which, ctypes.byref(v)), "mla_plan_query")
+        return int(v.value)
+
+    num_units = property(lambda self: self.query(0))
+    num_ctas = property(lambda self: self.query(1))
+    allowed_pairs = property(lambda self: self.query(4))
+    kv_tiles = property(lambda self: self.query(5))
+
+    def run(self, q, k, v, o=None, lse=None, return_lse=True, stream=None):
+        return mla_prefill_run(self, q, k, v, o, lse, return_lse, stream)
+
+    def status(self) -> int:
+        return mla_prefill_status(self)
+
+    def destroy(self):
+        if self._h:
+            h, self._h = self._h, None
+            _check(library().mla_plan_destroy(h), "mla_plan_destroy")
+
+    def __del__(self):
+        try:
+            if self._h and _lib is not None:
+                _lib.mla_plan_destroy(self._h)
+                self._h = None
+        except Exception:
+            pass
+
+
+def mla_prefill_plan(qo_indptr, kv_indptr, num_heads: int, head_dim_qk: int = 192, head_dim_vo: int = 128,
+                     causal: bool = True, sm_scale: float | None = None, window_left: int = -1,
+                     logits_soft_cap: float = 0.0, stream=None) -> PrefillPlan:
+    """Plan a ragged prefill (host indptrs).  ``sm_scale`` is required, as on the pages."""
+    if sm_scale is None:
+        raise ValueError("sm_scale must be given explicitly")
+    qo, kv = _host_i32(qo_indptr), _host_i32(kv_indptr)
+    if qo.ndim != 1 or kv.shape != qo.shape or qo.size < 1:
+        raise ValueError("qo_indptr and kv_indptr must be 1-D of equal length batch+1")
+    h = ctypes.c_void_p()
+    _check(library().mla_prefill_plan(ctypes.byref(h), _ptr(qo), _ptr(kv), qo.size - 1, num_heads, head_dim_qk,
+                                      head_dim_vo, int(bool(causal)), float(sm_scale), int(window_left),
+                                      float(logits_soft_cap), _stream(stream)), "mla_prefill_plan")
+    return PrefillPlan(h, num_heads, int(qo[-1]), int(kv[-1]))
+
+
+def mla_prefill_run(plan: PrefillPlan, q, k, v, o=None, lse=None, return_lse=True, stream=None):
+    """Run a plan; returns (o, lse) (lse None when not requested)."""
+    import torch
+    H = plan.num_heads
+    if tuple(q.shape) != (plan.total_q, H, 192):
+        raise ValueError(f"q must be [{plan.total_q}, {H}, 192], got {tuple(q.shape)}")
+    if tuple(k.shape) != (plan.total_kv, H, 192) or tuple(v.shape) != (plan.total_kv, H, 128):
+        raise ValueError("k/v shapes do not match the plan")
+    if o is None:
+        o = torch.empty((plan.total_q, H, 128), dtype=torch.bfloat16, device=q.device)
+    if return_lse and lse is None:
+        lse = torch.empty((plan.total_q, H), dtype=torch.float32, device=q.device)
+    if tuple(o.shape) != (plan.total_q, H, 128) or (lse is not None and tuple(lse.shape) != (plan.total_q, H)):
+        raise ValueError("o/lse shapes do not match the plan")
+    bf = torch.bfloat16
+    _check(library().mla_prefill_run(plan.handle, _dev(q, bf, "q"), _dev(k, bf, "k"), _dev(v, bf, "v"),
+                                     _dev(o, bf, "o"), _dev(lse, torch.float32, "lse"), _stream(stream)),
+           "mla_prefill_run")
+    return o, lse
+
+
+def mla_prefill_status(plan: PrefillPlan) -> int:
+    """Read-and-clear the plan's device status word; raises on a device-side error."""
+    code = library().mla_prefill_status(plan.handle)
+    _check(code, "mla_prefill_status")
+    return code
+
+
+def mla_plan_destroy(plan: PrefillPlan):
+    plan.destroy()
+
+
+def mla_plan_units_host(qo_indptr, kv_indptr, num_heads: int, causal: bool, window_left: int, num_ctas: int):
+    """Host planner only: returns (units [n, 8] int32, cta_offsets [num_ctas+1] int32)."""
+    qo, kv = _host_i32(qo_indptr), _host_i32(kv_indptr)
+    n = ctypes.c_int64(0)
+    offs = np.zeros(num_ctas + 1, dtype=np.int32)
+    lib = library()
+    args = (_ptr(qo), _ptr(kv), qo.size - 1, num_heads, int(bool(causal)), int(window_left), num_ctas)
+    code = lib.mla_plan_units_host(*args, None, 0, _ptr(offs), ctypes.byref(n))
+    if code not in (MLA_OK, -2):
+        _check(code, "mla_plan_units_host")
+    units = np.zeros((max(1, n.value), 8), dtype=np.int32)
+    _check(lib.mla_plan_units_host(*args, _ptr(units), n.value, _ptr(offs), ctypes.byref(n)),
+           "mla_plan_units_host")
+    return units[:n.value], offs
+
+
+# ---------------------------------------------------------------------------- gather / up-proj / merge
+def mla_gather_latent(cache, block_table, cu_seq_lens, chunk_starts, total_tokens: int, out=None, status=None,
+                      stream=None):
+    """Copy one prefix chunk out of the paged latent cache (device tensors)."""
+    import torch
+    nb, bs, e = cache.shape
+    if out is None:
+        out = torch.empty((total_tokens, e), dtype=cache.dtype, device=cache.device)
+    batch = block_table.shape[0]
+    i32 = torch.int32
+    _check(library().mla_gather_latent(_dev(cache, torch.bfloat16, "cache"), nb, bs, e,
+                                       _dev(block_table, i32, "block_table"), block_table.shape[1],
+                                       _dev(cu_seq_lens, i32, "cu_seq_lens"), _dev(chunk_starts, i32, "chunk_starts"),
+                                       batch, int(total_tokens), _dev(out, torch.bfloat16, "out"),
+                                       _dev(status, i32, "status"), _stream(stream)), "mla_gather_latent")
+    return out
+
+
+def mla_up_proj(latent, w_kvb, num_heads: int, k_out=None, v_out=None, status=None, stream=None):
+    """latent [T, 576] x w_kvb [512, H*256] -> K [T, H, 192], V [T, H, 128]."""
+    import torch
+    t = latent.shape[0]
+    if tuple(latent.shape[1:]) != (576,) or tuple(w_kvb.shape) != (512, num_heads * 256):
+        raise ValueError("latent must be [T, 576] and w_kvb [512, H*256]")
+    if k_out is None:
+        k_out = torch.empty((t, num_heads, 192), dtype=torch.bfloat16, device=latent.device)
+    if v_out is None:
+        v_out = torch.empty((t, num_heads, 128), dtype=torch.bfloat16, device=latent.device)
+    bf = torch.bfloat16
+    _check(library().mla_up_proj(_dev(latent, bf, "latent"), _dev(w_kvb, bf, "w_kvb"), t, num_heads,
+                                 _dev(k_out, bf, "k_out"), _dev(v_out, bf, "v_out"),
+                                 _dev(status, torch.int32, "status"), _stream(stream)), "mla_up_proj")
+    return k_out, v_out
+
+
+def mla_merge_state(o_a, lse_a, o_b, lse_b, o_out=None, lse_out=None, stream=None):
+    """Merge two partial states by LSE; o_out/lse_out may be o_a/lse_a (in place)."""
+    import torch
+    rows, h, d = o_a.shape
+    if o_out is None:
+        o_out = torch.empty_like(o_a)
+    if lse_out is None:
+        lse_out = torch.empty_like(lse_a)
+    bf, f32 = torch.bfloat16, torch.float32
+    _check(library().mla_merge_state(_dev(o_a, bf, "o_a"), _dev(lse_a, f32, "lse_a"), _dev(o_b, bf, "o_b"),
+                                     _dev(lse_b, f32, "lse_b"), _dev(o_out, bf, "o_out"),
+                                     _dev(lse_out, f32, "lse_out"), rows, h, d, _stream(stream)),
+           "mla_merge_state")
+    return o_out, lse_out

@@ -1,0 +1,367 @@
+// Ragged MLA prefill attention for sm_103a: O = softmax(sm_scale * Q K^T) V and the
+// per-row LSE, for query/key head dim 192 (128 NoPE + 64 RoPE) and value dim 128.
+//
+// What is computed follows vLLM "vllm.v1.attention.backends.mla.prefill.flashinfer"
+// (FlashInferPrefillBackend.finalize_attention_metadata: ragged qo/kv indptr, MHA,
+// causal for new tokens / non-causal for prefix chunks, sm_scale, window_left,
+// logits_soft_cap; FlashInferPrefillImpl.run_prefill_*: O and LSE per (row, head)).
+//
+// Design (one persistent CTA per SM, one work unit = 128 query rows of one head):
+//   warp 0      TMA producer: Q tile once per unit, then K and V tiles of 128 keys
+//               through two-stage rings (K and V released separately).
+//   warp 1      MMA issuer (one thread): S = Q K^T into one of two TMEM S buffers
+//               (tcgen05.mma, both operands from shared memory), then O += P V with P
+//               read from TMEM (written there by the softmax warps over the S buffer).
+//   warps 2-5   softmax: one thread per query row (= one TMEM lane).  Online softmax
+//               in base 2; O in TMEM is rescaled only when the running max grows by
+//               more than 2^8, so most tiles need no correction pass.  Epilogue
+//               normalises O, writes it (bf16) and the natural-log LSE (fp32).
+// Every pipeline wait is bounded: on time-out the CTA records MLA_DEVSTAT_TIMEOUT,
+// drains its own copies and MMAs, frees TMEM and returns.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tmem_wide.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int BM = kTileM;    // 128 query rows
+constexpr int BN = kTileN;    // 128 keys
+constexpr int PANEL = 128 * 64 * 2;   // one 128-row x 64-element bf16 panel, 128B swizzle
+constexpr int Q_PANELS = 3, K_PANELS = 3, V_PANELS = 2;
+constexpr int NSTAGE = 2;
+
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + Q_PANELS * PANEL;
+constexpr int OFF_V = OFF_K + NSTAGE * K_PANELS * PANEL;
+constexpr int OFF_BAR = OFF_V + NSTAGE * V_PANELS * PANEL;
+enum Bar { QF = 0, QE = 1, KF = 2, KE = 4, VF = 6, VE = 8, SF = 10, PF = 12, OD = 14, FIN = 15, NBAR = 16 };
+constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + slack for 1024-byte alignment
+
+constexpr int NTHREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+__device__ __forceinline__ constexpr uint32_t TM_S(int b) { return b ? 128u : 0u; }
+constexpr uint32_t TM_O = 256;
+
+constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false, false);
+constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, 128, false, true);
+
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;    // 2 s
+constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;    // 0.2 s
+constexpr float RESCALE_THRESHOLD = 8.0f;             // log2 units
+
+struct Ctx {
+  uint32_t sbase;
+  volatile int* abort_flag;
+  int* status;
+  __device__ uint32_t bar(int i) const { return sbase + OFF_BAR + 8 * i; }
+  __device__ bool wait(int b, uint32_t parity) const {
+    return mbar_wait_bounded(bar(b), parity, abort_flag, status, MLA_DEVSTAT_TIMEOUT, WAIT_LIMIT_NS);
+  }
+  __device__ void drain(int b, uint32_t parity) const {
+    int dummy = 0;
+    mbar_wait_bounded(bar(b), parity, &dummy, status, MLA_DEVSTAT_TIMEOUT, DRAIN_LIMIT_NS);
+  }
+};
+
+__device__ __forceinline__ Unit load_unit(const Unit* units, int i) {
+  const int4* p = reinterpret_cast<const int4*>(units + i);
+  int4 a = __ldg(p), b = __ldg(p + 1);
+  Unit u;
+  u.head = a.x; u.q_row0 = a.y; u.q_rows = a.z; u.q_pos0 = a.w;
+  u.kv_row0 = b.x; u.kv_len = b.y; u.diag = b.z; u.kv_tiles = b.w;
+  return u;
+}
+
+// ------------------------------------------------------------------ producer
+__device__ void run_producer(const Ctx& c, const PrefillParams& p, const CUtensorMap* tq,
+                             const CUtensorMap* tk, const CUtensorMap* tv, int ubeg, int uend) {
+  int q_g = 0, k_g = 0, v_g = 0;   // loads issued so far (Q tiles, K tiles, V tiles)
+  bool ok = true;
+  for (int ui = ubeg; ui < uend && ok; ++ui) {
+    const Unit u = load_unit(p.units, ui);
+    const int lo = u.kv_tiles & 0xFFFF, hi = (u.kv_tiles >> 16) & 0xFFFF;
+    if (hi <= lo) continue;
+    if (q_g > 0 && !c.wait(QE, (q_g - 1) & 1)) { ok = false; break; }
+    mbar_arrive_expect_tx(c.bar(QF), Q_PANELS * PANEL);
+    for (int i = 0; i < Q_PANELS; ++i)
+      tma_load_3d(c.sbase + OFF_Q + i * PANEL, tq, c.bar(QF), i * 64, u.head, u.q_row0);
+    ++q_g;
+    for (int t = lo; t < hi; ++t) {
+      const int row = u.kv_row0 + t * BN;
+      int s = k_g % NSTAGE;
+      uint32_t use = k_g / NSTAGE;
+      if (use > 0 && !c.wait(KE + s, (use - 1) & 1)) { ok = false; break; }
+      mbar_arrive_expect_tx(c.bar(KF + s), K_PANELS * PANEL);
+      for (int i = 0; i < K_PANELS; ++i)
+        tma_load_3d(c.sbase + OFF_K + (s * K_PANELS + i) * PANEL, tk, c.bar(KF + s), i * 64, u.head, row);
+      ++k_g;
+      s = v_g % NSTAGE;
+      use = v_g / NSTAGE;
+      if (use > 0 && !c.wait(VE + s, (use - 1) & 1)) { ok = false; break; }
+      mbar_arrive_expect_tx(c.bar(VF + s), V_PANELS * PANEL);
+      for (int i = 0; i < V_PANELS; ++i)
+        tma_load_3d(c.sbase + OFF_V + (s * V_PANELS + i) * PANEL, tv, c.bar(VF + s), i * 64, u.head, row);
+      ++v_g;
+    }
+  }
+  // Let every copy this thread started land before the CTA can exit: wait for the
+  // last phase issued on each barrier (already complete on the normal path).
+  if (q_g > 0) c.drain(QF, (q_g - 1) & 1);
+  for (int s = 0; s < NSTAGE; ++s) {
+    if (k_g > s) c.drain(KF + s, (((k_g - 1 - s) / NSTAGE)) & 1);
+    if (v_g > s) c.drain(VF + s, (((v_g - 1 - s) / NSTAGE)) & 1);
+  }
+}
+
+// ------------------------------------------------------------------ MMA issuer
+__device__ void run_mma(const Ctx& c, const PrefillParams& p, uint32_t tmem, int ubeg, int uend) {
+  int q_g = 0, kv_g = 0, s_g = 0;
+  bool ok = true;
+  auto issue_pv = [&](int t_local, int kv_base, int s_base) -> bool {
+    const int sg = s_base + t_local, b = sg & 1;
+    if (!c.wait(PF + b, (sg >> 1) & 1)) return false;
+    const int g = kv_base + t_local, s = g % NSTAGE;
+    if (!c.wait(VF + s, (g / NSTAGE) & 1)) return false;
+    tc_fence_after();
+    const uint32_t vbase = c.sbase + OFF_V + s * V_PANELS * PANEL;
+#pragma unroll
+    for (int kk = 0; kk < BN / 16; ++kk) {
+      const uint64_t bd = sdesc_sw128(vbase + kk * 16 * 128, PANEL, 1024);
+      mma_ts(tmem + TM_O, tmem + TM_S(b) + kk * 8, bd, IDESC_PV, (t_local > 0 || kk > 0) ? 1u : 0u);
+    }
+    tc_commit(c.bar(VE + s));
+    tc_commit(c.bar(OD));
+    return true;
+  };
+  for (int ui = ubeg; ui < uend && ok; ++ui) {
+    const Unit u = load_unit(p.units, ui);
+    const int lo = u.kv_tiles & 0xFFFF, hi = (u.kv_tiles >> 16) & 0xFFFF;
+    const int n = hi - lo;
+    if (n <= 0) continue;
+    if (!c.wait(QF, q_g & 1)) { ok = false; break; }
+    ++q_g;
+    tc_fence_after();
+    for (int j = 0; j < n && ok; ++j) {
+      const int g = kv_g + j, s = g % NSTAGE;
+      if (!c.wait(KF + s, (g / NSTAGE) & 1)) { ok = false; break; }
+      tc_fence_after();
+      const int b = (s_g + j) & 1;
+      const uint32_t kbase = c.sbase + OFF_K + s * K_PANELS * PANEL;
+#pragma unroll
+      for (int kk = 0; kk < 192 / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * PANEL + (kk & 3) * 32;
+        const uint64_t ad = sdesc_sw128(c.sbase + OFF_Q + off, 16, 1024);
+        const uint64_t bd = sdesc_sw128(kbase + off, 16, 1024);
+        mma_ss(tmem + TM_S(b), ad, bd, IDESC_QK, kk > 0 ? 1u : 0u);
+      }
+      tc_commit(c.bar(SF + b));
+      tc_commit(c.bar(KE + s));
+      if (j == n - 1) tc_commit(c.bar(QE));
+      if (j > 0 && !issue_pv(j - 1, kv_g, s_g)) { ok = false; break; }
+    }
+    if (ok && !issue_pv(n - 1, kv_g, s_g)) ok = false;
+    kv_g += n;
+    s_g += n;
+  }
+  // Every MMA issued by this thread must finish before TMEM is released.
+  tc_commit(c.bar(FIN));
+  c.drain(FIN, 0);
+}
+
+// ------------------------------------------------------------------ softmax
+__device__ void run_softmax(const Ctx& c, const PrefillParams& p, uint32_t tmem, int ubeg, int uend) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quad = warp & 3;                 // TMEM lanes this warp may touch
+  const int row = quad * 32 + lane;
+  const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
+  int s_g = 0, od_g = 0;
+  bool ok = true;
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  for (int ui = ubeg; ui < uend && ok; ++ui) {
+    const Unit u = load_unit(p.units, ui);
+    const int lo = u.kv_tiles & 0xFFFF, hi = (u.kv_tiles >> 16) & 0xFFFF;
+    const int n = hi - lo;
+    const bool row_ok = row < u.q_rows;
+    const int qpos = u.q_pos0 + row;
+    const size_t orow = (size_t)(u.q_row0 + row) * p.num_heads + u.head;
+    if (n <= 0) {
+      if (row_ok) {
+        uint4* dst = reinterpret_cast<uint4*>(p.o + orow * 128);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+        if (p.lse) p.lse[orow] = NEG_INF;
+      }
+      continue;
+    }
+    // Per-row key window inside the request: allowed positions [klo, khi).
+    const int khi = p.causal ? min(u.kv_len, qpos + u.diag + 1) : u.kv_len;
+    const int klo = p.window_left >= 0 ? max(0, qpos + u.diag - p.window_left) : 0;
+    float m_used = NEG_INF, l = 0.f;
+    for (int j = 0; j < n; ++j) {
+      const int sg = s_g + j, b = sg & 1;
+      if (!__all_sync(0xffffffffu, c.wait(SF + b, (sg >> 1) & 1))) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sr[128];
+      tmem_ld128_sync(lane_addr + TM_S(b), sr);
+      float* t = reinterpret_cast<float*>(sr);
+      if (p.has_cap) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) t[i] = p.cap_log2 * tanhf(t[i] * p.x_to_cap);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) t[i] *= p.scale_log2;
+      }
+      const int kp0 = (lo + j) * BN;
+      const int c_hi = khi - kp0, c_lo = klo - kp0;
+      if (c_hi < BN || c_lo > 0) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i >= c_hi || i < c_lo) t[i] = NEG_INF;
+      }
+      float mx = t[0];
+#pragma unroll
+      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, t[i]);
+      float m_new = m_used;
+      bool rescale = false;
+      if (j == 0) {
+        m_new = mx;
+      } else if (mx > m_used + RESCALE_THRESHOLD) {
+        m_new = mx;
+        rescale = true;
+      }
+      const float msub = (m_new == NEG_INF) ? 0.f : m_new;
+      float sum = 0.f;
+      uint32_t pr[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const float p0 = ex2_approx(t[2 * i] - msub);
+        const float p1 = ex2_approx(t[2 * i + 1] - msub);
+        sum += p0 + p1;
+        pr[i] = pack_bf16x2(p0, p1);
+      }
+      tmem_st64_sync(lane_addr + TM_S(b), pr);
+      float alpha = 1.f;
+      if (j > 0) {
+        // O must hold P_{j-1} V_{j-1} before it may be rescaled.
+        if (!__all_sync(0xffffffffu, c.wait(OD, od_g & 1))) { ok = false; break; }
+        ++od_g;
+        tc_fence_after();
+        if (rescale) alpha = ex2_approx(m_used - m_new);
+        // tcgen05.ld/st are warp-collective (.sync.aligned): the whole warp rescales
+        // its 32 rows together, rows that keep their max with alpha = 1.
+        if (__any_sync(0xffffffffu, rescale)) {
+          uint32_t orr[128];
+          tmem_ld128_sync(lane_addr + TM_O, orr);
+#pragma unroll
+          for (int i = 0; i < 128; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+          tmem_st128_sync(lane_addr + TM_O, orr);
+        }
+      }
+      l = l * alpha + sum;
+      m_used = m_new;
+      tc_fence_before();
+      mbar_arrive(c.bar(PF + b));
+    }
+    if (!ok) break;
+    if (!__all_sync(0xffffffffu, c.wait(OD, od_g & 1))) { ok = false; break; }
+    ++od_g;
+    tc_fence_after();
+    uint32_t orr[128];
+    tmem_ld128_sync(lane_addr + TM_O, orr);
+    tc_fence_before();
+    if (row_ok) {
+      const bool empty = !(l > 0.f);
+      const float inv = empty ? 0.f : 1.f / l;
+      uint4* dst = reinterpret_cast<uint4*>(p.o + orow * 128);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        uint4 w;
+        w.x = pack_bf16x2(__uint_as_float(orr[8 * i + 0]) * inv, __uint_as_float(orr[8 * i + 1]) * inv);
+        w.y = pack_bf16x2(__uint_as_float(orr[8 * i + 2]) * inv, __uint_as_float(orr[8 * i + 3]) * inv);
+        w.z = pack_bf16x2(__uint_as_float(orr[8 * i + 4]) * inv, __uint_as_float(orr[8 * i + 5]) * inv);
+        w.w = pack_bf16x2(__uint_as_float(orr[8 * i + 6]) * inv, __uint_as_float(orr[8 * i + 7]) * inv);
+        dst[i] = w;
+      }
+      if (p.lse) {
+        float lg;
+        asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(l));
+        p.lse[orow] = empty ? NEG_INF : (m_used + lg) * 0.6931471805599453f;
+      }
+    }
+    s_g += n;
+  }
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  int* abort_flag = reinterpret_cast<int*>(smem + OFF_MISC + 4);
+  Ctx c{smem_addr(smem), abort_flag, p.status};
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NBAR; ++i) mbar_init(c.bar(i), 1);
+    mbar_init(c.bar(PF + 0), 128);
+    mbar_init(c.bar(PF + 1), 128);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int ubeg = p.cta_offsets[blockIdx.x], uend = p.cta_offsets[blockIdx.x + 1];
+
+  if (warp == 0) {
+    if (lane == 0) run_producer(c, p, &tm_q, &tm_k, &tm_v, ubeg, uend);
+  } else if (warp == 1) {
+    if (lane == 0) run_mma(c, p, tmem, ubeg, uend);
+  } else {
+    run_softmax(c, p, tmem, ubeg, uend);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+int prefill_smem_bytes() { return SMEM_BYTES; }
+
+cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const PrefillParams& p, int num_ctas, cudaStream_t stream) {
+  static int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  prefill_kernel<<<num_ctas, NTHREADS, SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -1,0 +1,275 @@
+// C ABI of the library (declared in include/mla_prefill.h): argument checks, the
+// plan object and its device workspace, tensor maps, kernel launches.
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "internal.h"
+
+using namespace mla;
+
+struct mla_plan {
+  int device = 0;
+  int batch = 0, num_heads = 0, causal = 0, window_left = -1;
+  float sm_scale = 0.f, soft_cap = 0.f;
+  int64_t total_q = 0, total_kv = 0;
+  PlanResult plan;
+  int num_ctas = 0;
+  void* workspace = nullptr;     // units | cta offsets | status word
+  Unit* d_units = nullptr;
+  int32_t* d_offsets = nullptr;
+  int* d_status = nullptr;
+};
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_error_string(int status) {
+  switch (status) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID_ARG: return "invalid argument";
+    case MLA_ERR_SHAPE: return "inconsistent shapes or indptr";
+    case MLA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MLA_ERR_CUDA: return "CUDA error";
+    case MLA_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
+    case MLA_ERR_DEVICE_BOUNDS: return "device index out of range";
+    default: return "unknown status";
+  }
+}
+
+int mla_abi_version(void) { return 1; }
+
+int mla_plan_units_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int batch, int num_heads,
+                        int causal, int window_left, int num_ctas, int32_t* units, int64_t capacity,
+                        int32_t* cta_offsets, int64_t* num_units) {
+  if (!num_units || !cta_offsets || (capacity > 0 && !units) || num_ctas < 1) return MLA_ERR_INVALID_ARG;
+  PlanResult pr;
+  const int rc = build_plan(qo_indptr, kv_indptr, batch, num_heads, causal != 0, window_left, num_ctas, &pr);
+  if (rc != MLA_OK) return rc;
+  *num_units = (int64_t)pr.units.size();
+  if ((int64_t)pr.units.size() > capacity) return MLA_ERR_SHAPE;
+  if (!pr.units.empty()) std::memcpy(units, pr.units.data(), pr.units.size() * sizeof(Unit));
+  const int used = (int)pr.cta_offsets.size() - 1;
+  for (int c = 0; c <= num_ctas; ++c)
+    cta_offsets[c] = c <= used ? pr.cta_offsets[c] : (int32_t)pr.units.size();
+  return MLA_OK;
+}
+
+int mla_prefill_plan(mla_plan_t* out, const int32_t* qo_indptr, const int32_t* kv_indptr, int batch,
+                     int num_heads, int head_dim_qk, int head_dim_vo, int causal, float sm_scale,
+                     int window_left, float logits_soft_cap, void* stream) {
+  if (!out) return MLA_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!qo_indptr || !kv_indptr || batch < 0 || num_heads < 1 || num_heads > 65535) return MLA_ERR_INVALID_ARG;
+  if (head_dim_qk != 192 || head_dim_vo != 128) return MLA_ERR_UNSUPPORTED;
+  if (!std::isfinite(sm_scale) || !std::isfinite(logits_soft_cap) || window_left < -1) return MLA_ERR_INVALID_ARG;
+  // Shape checks first (host only), so a bad call never touches the device.
+  {
+    PlanResult probe;
+    const int rc = build_plan(qo_indptr, kv_indptr, batch, num_heads, causal != 0, window_left, 1, &probe);
+    if (rc != MLA_OK) return rc;
+  }
+  const int sms = device_sm_count();
+  if (sms <= 0) return MLA_ERR_CUDA;
+
+  mla_plan* p = new (std::nothrow) mla_plan();
+  if (!p) return MLA_ERR_CUDA;
+  int rc = build_plan(qo_indptr, kv_indptr, batch, num_heads, causal != 0, window_left, sms, &p->plan);
+  if (rc != MLA_OK) { delete p; return rc; }
+  cudaGetDevice(&p->device);
+  p->batch = batch;
+  p->num_heads = num_heads;
+  p->causal = causal != 0;
+  p->window_left = window_left;
+  p->sm_scale = sm_scale;
+  p->soft_cap = logits_soft_cap > 0.f ? logits_soft_cap : 0.f;
+  p->total_q = qo_indptr[batch];
+  p->total_kv = kv_indptr[batch];
+  p->num_ctas = (int)p->plan.cta_offsets.size() - 1;
+
+  const size_t units_bytes = round_up(std::max<size_t>(1, p->plan.units.size()) * sizeof(Unit), 256);
+  const size_t offs_bytes = round_up(p->plan.cta_offsets.size() * sizeof(int32_t), 256);
+  if (cudaMalloc(&p->workspace, units_bytes + offs_bytes + 256) != cudaSuccess) {
+    delete p;
+    return MLA_ERR_CUDA;
+  }
+  char* ws = static_cast<char*>(p->workspace);
+  p->d_units = reinterpret_cast<Unit*>(ws);
+  p->d_offsets = reinterpret_cast<int32_t*>(ws + units_bytes);
+  p->d_status = reinterpret_cast<int*>(ws + units_bytes + offs_bytes);
+  cudaStream_t s = as_stream(stream);
+  cudaError_t e = cudaSuccess;
+  if (!p->plan.units.empty())
+    e = cudaMemcpyAsync(p->d_units, p->plan.units.data(), p->plan.units.size() * sizeof(Unit),
+                        cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(p->d_offsets, p->plan.cta_offsets.data(), p->plan.cta_offsets.size() * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(p->d_status, 0, sizeof(int), s);
+  if (e != cudaSuccess) {
+    cudaFree(p->workspace);
+    delete p;
+    return MLA_ERR_CUDA;
+  }
+  *out = p;
+  return MLA_OK;
+}
+
+int mla_prefill_run(mla_plan_t p, const void* q, const void* k, const void* v, void* o, float* lse,
+                    void* stream) {
+  if (!p) return MLA_ERR_INVALID_ARG;
+  if (p->plan.units.empty()) return MLA_OK;   // no query rows
+  if (!q || !o || !aligned16(q) || !aligned16(o) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return MLA_ERR_INVALID_ARG;
+  if (p->total_kv > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return MLA_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != p->device) return MLA_ERR_INVALID_ARG;
+
+  // With no key rows at all no K/V tile is ever loaded; the maps still need a valid base.
+  const void* kb = p->total_kv > 0 ? k : q;
+  const void* vb = p->total_kv > 0 ? v : q;
+  const uint64_t H = (uint64_t)p->num_heads;
+  const uint64_t kv_rows = p->total_kv > 0 ? (uint64_t)p->total_kv : 1;
+  CUtensorMap tq, tk, tv;
+  const uint32_t box[3] = {64, 1, 128};
+  {
+    const uint64_t dims[3] = {192, H, (uint64_t)p->total_q};
+    const uint64_t strides[2] = {192 * 2, H * 192 * 2};
+    if (make_tensor_map_bf16(&tq, q, 3, dims, strides, box) != MLA_OK) return MLA_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {192, H, kv_rows};
+    const uint64_t strides[2] = {192 * 2, H * 192 * 2};
+    if (make_tensor_map_bf16(&tk, kb, 3, dims, strides, box) != MLA_OK) return MLA_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {128, H, kv_rows};
+    const uint64_t strides[2] = {128 * 2, H * 128 * 2};
+    if (make_tensor_map_bf16(&tv, vb, 3, dims, strides, box) != MLA_OK) return MLA_ERR_CUDA;
+  }
+  PrefillParams prm;
+  prm.units = p->d_units;
+  prm.cta_offsets = p->d_offsets;
+  prm.status = p->d_status;
+  prm.o = static_cast<__nv_bfloat16*>(o);
+  prm.lse = lse;
+  prm.num_heads = p->num_heads;
+  prm.causal = p->causal;
+  prm.window_left = p->window_left;
+  const float LOG2E = 1.4426950408889634f;
+  prm.has_cap = p->soft_cap > 0.f;
+  prm.scale_log2 = p->sm_scale * LOG2E;
+  prm.cap_log2 = prm.has_cap ? p->soft_cap * LOG2E : 0.f;
+  prm.x_to_cap = prm.has_cap ? p->sm_scale / p->soft_cap : 0.f;
+  return launch_prefill(tq, tk, tv, prm, p->num_ctas, as_stream(stream)) == cudaSuccess ? MLA_OK
+                                                                                     : MLA_ERR_CUDA;
+}
+
+int mla_prefill_status(mla_plan_t p) {
+  if (!p) return MLA_ERR_INVALID_ARG;
+  int word = 0;
+  if (cudaMemcpy(&word, p->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
+  if (word != 0 && cudaMemset(p->d_status, 0, sizeof(int)) != cudaSuccess) return MLA_ERR_CUDA;
+  if (word & MLA_DEVSTAT_TIMEOUT) return MLA_ERR_DEVICE_TIMEOUT;
+  if (word & MLA_DEVSTAT_BAD_INDEX) return MLA_ERR_DEVICE_BOUNDS;
+  return MLA_OK;
+}
+
+int mla_plan_destroy(mla_plan_t p) {
+  if (!p) return MLA_OK;
+  int rc = MLA_OK;
+  if (p->workspace) {
+    if (cudaDeviceSynchronize() != cudaSuccess) rc = MLA_ERR_CUDA;
+    if (cudaFree(p->workspace) != cudaSuccess) rc = MLA_ERR_CUDA;
+  }
+  delete p;
+  return rc;
+}
+
+int mla_plan_query(mla_plan_t p, int which, int64_t* value) {
+  if (!p || !value) return MLA_ERR_INVALID_ARG;
+  switch (which) {
+    case 0: *value = (int64_t)p->plan.units.size(); break;
+    case 1: *value = p->num_ctas; break;
+    case 2: *value = p->total_q; break;
+    case 3: *value = p->total_kv; break;
+    case 4: *value = p->plan.allowed_pairs; break;
+    case 5: *value = p->plan.kv_tiles; break;
+    default: return MLA_ERR_INVALID_ARG;
+  }
+  return MLA_OK;
+}
+
+int mla_gather_latent(const void* cache, int64_t num_blocks, int block_size, int entry_dim,
+                      const int32_t* block_table, int max_blocks_per_req, const int32_t* cu_seq_lens,
+                      const int32_t* chunk_starts, int batch, int64_t total_tokens, void* out,
+                      int32_t* status, void* stream) {
+  if (total_tokens < 0 || batch < 0 || num_blocks < 0 || block_size < 1 || entry_dim < 8 ||
+      entry_dim % 8 != 0 || max_blocks_per_req < 0)
+    return MLA_ERR_INVALID_ARG;
+  if (total_tokens == 0) return MLA_OK;
+  if (batch == 0) return MLA_ERR_SHAPE;
+  if (!cache || !block_table || !cu_seq_lens || !chunk_starts || !out || !aligned16(cache) || !aligned16(out))
+    return MLA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(status) & 3u) != 0) return MLA_ERR_INVALID_ARG;
+  return launch_gather(cache, num_blocks, block_size, entry_dim, block_table, max_blocks_per_req,
+                       cu_seq_lens, chunk_starts, batch, total_tokens, out, status,
+                       as_stream(stream)) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
+int mla_up_proj(const void* latent, const void* w_kvb, int64_t num_tokens, int num_heads, void* k_out,
+                void* v_out, int32_t* status, void* stream) {
+  if (num_tokens < 0 || num_heads < 1) return MLA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return MLA_OK;
+  if (num_tokens > (int64_t)1 << 31) return MLA_ERR_UNSUPPORTED;
+  if (!latent || !w_kvb || !k_out || !v_out || !aligned16(latent) || !aligned16(w_kvb) ||
+      !aligned16(k_out) || !aligned16(v_out))
+    return MLA_ERR_INVALID_ARG;
+  if (((num_tokens + 127) / 128) * (int64_t)num_heads > 0x7fffffff) return MLA_ERR_UNSUPPORTED;
+  CUtensorMap ta, tb;
+  {
+    const uint64_t dims[2] = {576, (uint64_t)num_tokens};
+    const uint64_t strides[1] = {576 * 2};
+    const uint32_t box[2] = {64, 128};
+    if (make_tensor_map_bf16(&ta, latent, 2, dims, strides, box) != MLA_OK) return MLA_ERR_CUDA;
+  }
+  {
+    const uint64_t n = (uint64_t)num_heads * 256;
+    const uint64_t dims[2] = {n, 512};
+    const uint64_t strides[1] = {n * 2};
+    const uint32_t box[2] = {64, 64};
+    if (make_tensor_map_bf16(&tb, w_kvb, 2, dims, strides, box) != MLA_OK) return MLA_ERR_CUDA;
+  }
+  return launch_up_proj(ta, tb, latent, num_tokens, num_heads, k_out, v_out, status, as_stream(stream)) ==
+                 cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
+int mla_merge_state(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o_out,
+                    float* lse_out, int64_t rows, int num_heads, int head_dim, void* stream) {
+  if (rows < 0 || num_heads < 1) return MLA_ERR_INVALID_ARG;
+  if (head_dim < 8 || head_dim > 256 || (head_dim & (head_dim - 1)) != 0) return MLA_ERR_UNSUPPORTED;
+  if (rows == 0) return MLA_OK;
+  if (!o_a || !o_b || !lse_a || !lse_b || !o_out || !aligned16(o_a) || !aligned16(o_b) || !aligned16(o_out))
+    return MLA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(lse_a) | reinterpret_cast<uintptr_t>(lse_b) |
+       reinterpret_cast<uintptr_t>(lse_out)) & 3u)
+    return MLA_ERR_INVALID_ARG;
+  return launch_merge(o_a, lse_a, o_b, lse_b, o_out, lse_out, rows, num_heads, head_dim, as_stream(stream)) ==
+                 cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
+}  // extern "C"

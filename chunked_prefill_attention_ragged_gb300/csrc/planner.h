@@ -1,0 +1,40 @@
+// Host planner for ragged prefill attention: cuts every (request, head) into
+// 128-row query tiles, gives each tile the range of 128-key tiles that hold at
+// least one allowed key, and spreads the tiles over a persistent grid.
+#pragma once
+#include <cstdint>
+#include <vector>
+
+namespace mla {
+
+constexpr int kTileM = 128;   // query rows per tile
+constexpr int kTileN = 128;   // keys per tile
+
+// One work unit = one query tile of one head.  32 bytes, read by the kernel.
+struct Unit {
+  int32_t head;
+  int32_t q_row0;     // global row of the tile's first query
+  int32_t q_rows;     // valid query rows in the tile (1..128)
+  int32_t q_pos0;     // position of the first query inside its request
+  int32_t kv_row0;    // global row of the request's first key
+  int32_t kv_len;     // keys of the request
+  int32_t diag;       // kv_len - q_len: query position p sits at key position p + diag
+  int32_t kv_tiles;   // kv tile range: lo | hi << 16, tiles [lo, hi) of 128 keys
+};
+static_assert(sizeof(Unit) == 32, "unit layout");
+
+inline int unit_tile_lo(const Unit& u) { return u.kv_tiles & 0xFFFF; }
+inline int unit_tile_hi(const Unit& u) { return (u.kv_tiles >> 16) & 0xFFFF; }
+
+struct PlanResult {
+  std::vector<Unit> units;        // execution order, grouped per CTA
+  std::vector<int32_t> cta_offsets;  // num_ctas + 1
+  int64_t allowed_pairs = 0;      // sum over requests of allowed (query, key) pairs
+  int64_t kv_tiles = 0;           // sum over units of (hi - lo)
+};
+
+// Returns 0 or a negative MLA_ERR_* code.  Inputs are validated here.
+int build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr, int batch, int num_heads,
+               bool causal, int window_left, int max_ctas, PlanResult* out);
+
+}  // namespace mla

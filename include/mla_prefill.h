@@ -1,0 +1,203 @@
+/*
+ * mla_prefill.h -- C ABI of the GB300 (sm_103a) MLA ragged prefill library.
+ *
+ * The operations follow these pages:
+ *   [vLLM-FI]  vLLM API docs, "vllm.v1.attention.backends.mla.prefill.flashinfer":
+ *              FlashInferPrefillBackend.finalize_attention_metadata (plan of a
+ *              causal ragged problem over the new tokens and of one non-causal
+ *              problem per prefix chunk, with head_dim_qk = 128 NoPE + 64 RoPE,
+ *              head_dim_vo = 128, explicit sm_scale, window_left,
+ *              logits_soft_cap) and FlashInferPrefillImpl.run_prefill_new_tokens /
+ *              run_prefill_context_chunk (run(q, k, v, return_lse) -> O, LSE with
+ *              LSE laid out (q_len, num_heads)).
+ *   [sglang]   sglang issue #3849, "[DeepseekR1] How ragged prefill manage
+ *              kv_cache?": prefill attention is MHA with 192-dim Q/K and 128-dim V
+ *              while the cache keeps 512 latent + 64 rope per token.
+ *   [TVM]      Apache TVM PR #17674, "[KVCache] PagedKVCache refactor, FlashInfer
+ *              JIT and MLA integration": sm_scale is always passed explicitly.
+ *   [vLLM-V4]  vLLM "vllm/models/deepseek_v4/sparse_mla.py",
+ *              _build_c128a_topk_metadata_kernel (decode branch): the paged
+ *              slot rule block_table[r, pos / block_size] * block_size +
+ *              pos % block_size.
+ *
+ * Conventions for every entry point:
+ *   - Return value: MLA_OK (0) or a negative MLA_ERR_* code; nothing aborts,
+ *     throws or prints.  mla_error_string() names a code.
+ *   - Tensors are caller-owned, contiguous, row-major device memory (bf16 as
+ *     raw 16-bit storage, fp32 LSE).  Device pointers must be 16-byte aligned
+ *     (MLA_ERR_INVALID_ARG otherwise).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Device work is enqueued asynchronously on it; argument
+ *     checks happen on the host before anything is enqueued, so an error
+ *     return means nothing was launched.
+ *   - Only the plan call allocates (its own device workspace).  The run,
+ *     gather, up-projection and merge calls allocate nothing.
+ *   - Device-side problems (a block id outside the cache, a pipeline wait
+ *     that timed out) never fault the GPU: the kernel skips the access,
+ *     records a flag in a status word and returns.
+ */
+#ifndef MLA_PREFILL_H_
+#define MLA_PREFILL_H_
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define MLA_OK                  0
+#define MLA_ERR_INVALID_ARG    -1   /* null/misaligned pointer, bad scalar   */
+#define MLA_ERR_SHAPE          -2   /* indptr not monotone, sizes disagree   */
+#define MLA_ERR_UNSUPPORTED    -3   /* head dims other than 192/128, etc.    */
+#define MLA_ERR_CUDA           -4   /* a CUDA runtime/driver call failed     */
+#define MLA_ERR_DEVICE_TIMEOUT -5   /* a kernel pipeline wait gave up        */
+#define MLA_ERR_DEVICE_BOUNDS  -6   /* a kernel met an out-of-range index    */
+
+/* bits a kernel may set in a device status word */
+#define MLA_DEVSTAT_TIMEOUT    0x1
+#define MLA_DEVSTAT_BAD_INDEX  0x2
+
+/* Name of a status code ("ok", "invalid argument", ...).  Never NULL. */
+MLA_API const char* mla_error_string(int status);
+
+/* ABI version, currently 1. */
+MLA_API int mla_abi_version(void);
+
+/* ======================================================================
+ * Ragged prefill attention: plan once per batch, run once per layer.
+ * [vLLM-FI] finalize_attention_metadata / run_prefill_*; [TVM] sm_scale.
+ * ====================================================================== */
+typedef struct mla_plan* mla_plan_t;
+
+/*
+ * Plan a ragged prefill problem.
+ *   qo_indptr, kv_indptr : HOST int32 arrays of batch+1 prefix sums
+ *       (qo_indptr[0] = kv_indptr[0] = 0, non-decreasing).  Request r owns
+ *       query rows [qo_indptr[r], qo_indptr[r+1]) and key rows
+ *       [kv_indptr[r], kv_indptr[r+1]).
+ *   num_heads            : query heads = KV heads (MHA), >= 1.
+ *   head_dim_qk          : must be 192 (128 NoPE + 64 RoPE), else MLA_ERR_UNSUPPORTED.
+ *   head_dim_vo          : must be 128, else MLA_ERR_UNSUPPORTED.
+ *   causal               : nonzero = causal, aligned bottom-right (query row i
+ *       of a request sits at key position i + Lkv - Lq).
+ *   sm_scale             : logits are sm_scale * q.k (finite, required).
+ *   window_left          : -1 = none; w >= 0 keeps keys with position
+ *       >= i + Lkv - Lq - w.  Values below -1 are invalid.
+ *   logits_soft_cap      : <= 0 = none; c > 0 replaces a logit x by
+ *       c * tanh(x / c) (after sm_scale).
+ *   stream               : the plan's work list is uploaded asynchronously
+ *       on this stream; runs on other streams must be ordered after it.
+ * On success *out owns a device workspace (work list + status word) until
+ * mla_plan_destroy.  Rows that see no key produce O = 0 and LSE = -inf.
+ */
+MLA_API int mla_prefill_plan(mla_plan_t* out, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                     int batch, int num_heads, int head_dim_qk, int head_dim_vo, int causal,
+                     float sm_scale, int window_left, float logits_soft_cap, void* stream);
+
+/*
+ * Run a planned problem ("NHD" ragged layout).
+ *   q   : bf16 [qo_indptr[batch], num_heads, 192]
+ *   k   : bf16 [kv_indptr[batch], num_heads, 192]
+ *   v   : bf16 [kv_indptr[batch], num_heads, 128]
+ *   o   : bf16 [qo_indptr[batch], num_heads, 128]            (written)
+ *   lse : fp32 [qo_indptr[batch], num_heads], natural log, or NULL to skip.
+ * Allocates nothing and does not synchronise; safe to capture in a CUDA
+ * graph.  Kernel-side failures are reported by mla_prefill_status.
+ */
+MLA_API int mla_prefill_run(mla_plan_t plan, const void* q, const void* k, const void* v, void* o,
+                    float* lse, void* stream);
+
+/*
+ * Read and clear the plan's device status word (a blocking device-to-host
+ * copy; call after the run's stream has completed).  Returns MLA_OK,
+ * MLA_ERR_DEVICE_TIMEOUT or MLA_ERR_CUDA.
+ */
+MLA_API int mla_prefill_status(mla_plan_t plan);
+
+/* Release the plan and its workspace (synchronises the device).  NULL is a no-op. */
+MLA_API int mla_plan_destroy(mla_plan_t plan);
+
+/* Plan facts: which = 0 work units, 1 CTAs launched, 2 total query rows,
+ * 3 total key rows, 4 allowed (query, key) pairs summed over requests (one head),
+ * 5 KV tiles summed over units. */
+MLA_API int mla_plan_query(mla_plan_t plan, int which, int64_t* value);
+
+/*
+ * Host-only planner (no CUDA call), for inspection and tests.  Same
+ * arguments as mla_prefill_plan plus `num_ctas` (the persistent grid).
+ * Writes at most `capacity` units as 8 int32 each:
+ *   {head, q_row0, q_rows, q_pos0, kv_row0, kv_len, diag, kv_tile_lo | kv_tile_hi << 16}
+ * in execution order, and cta_offsets[num_ctas+1] (CTA c runs units
+ * [cta_offsets[c], cta_offsets[c+1])).  *num_units receives the count even
+ * when capacity is too small (then MLA_ERR_SHAPE is returned).
+ */
+MLA_API int mla_plan_units_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int batch,
+                        int num_heads, int causal, int window_left, int num_ctas,
+                        int32_t* units, int64_t capacity, int32_t* cta_offsets,
+                        int64_t* num_units);
+
+/* ======================================================================
+ * Paged latent gather.  [vLLM-V4] slot rule; [sglang] 512 latent + 64 rope
+ * per cache row; [vLLM-FI] chunk i's kv_indptr = chunked_context.cu_seq_lens[i].
+ * ====================================================================== */
+/*
+ *   cache        : bf16 [num_blocks, block_size, entry_dim] (entry_dim % 8 == 0; 576 for MLA)
+ *   block_table  : DEVICE int32 [batch, max_blocks_per_req]
+ *   cu_seq_lens  : DEVICE int32 [batch+1], this chunk's kv_indptr
+ *   chunk_starts : DEVICE int32 [batch], first prefix position of the chunk per request
+ *   total_tokens : host copy of cu_seq_lens[batch] (rows of `out`)
+ *   out          : bf16 [total_tokens, entry_dim]; row cu_seq_lens[r] + t is
+ *                  position chunk_starts[r] + t of request r
+ *   status       : DEVICE int32 word or NULL; MLA_DEVSTAT_BAD_INDEX is OR-ed in when a
+ *                  row's block id is outside [0, num_blocks) or its table slot is past
+ *                  max_blocks_per_req (that row is written as zeros).
+ * Bit-exact copy; allocates nothing.
+ */
+MLA_API int mla_gather_latent(const void* cache, int64_t num_blocks, int block_size, int entry_dim,
+                      const int32_t* block_table, int max_blocks_per_req,
+                      const int32_t* cu_seq_lens, const int32_t* chunk_starts, int batch,
+                      int64_t total_tokens, void* out, int32_t* status, void* stream);
+
+/* ======================================================================
+ * Latent up-projection.  [sglang] 512 latent + 64 rope -> MHA K (192) / V (128).
+ * ====================================================================== */
+/*
+ *   latent : bf16 [num_tokens, 576] (512 latent then 64 rope), e.g. gather output
+ *   w_kvb  : bf16 [512, num_heads * 256]; columns h*256 + [0,128) give head h's
+ *            K_nope, h*256 + [128,256) its V
+ *   k_out  : bf16 [num_tokens, num_heads, 192] = [latent[:, :512] @ W_knope(h) || rope]
+ *   v_out  : bf16 [num_tokens, num_heads, 128] = latent[:, :512] @ W_v(h)
+ *   status : DEVICE int32 word or NULL; MLA_DEVSTAT_TIMEOUT is OR-ed in if a pipeline
+ *            wait of the kernel gave up (outputs are then incomplete).
+ * fp32 accumulation on tensor cores, one rounding to bf16.  Allocates nothing.
+ */
+MLA_API int mla_up_proj(const void* latent, const void* w_kvb, int64_t num_tokens, int num_heads,
+                void* k_out, void* v_out, int32_t* status, void* stream);
+
+/* ======================================================================
+ * LSE merge of two partial attention states.  [vLLM-FI]
+ * run_prefill_context_chunk always returns LSE so chunk results can merge.
+ * ====================================================================== */
+/*
+ *   o_a, o_b : bf16 [rows, num_heads, head_dim]; lse_a, lse_b : fp32 [rows, num_heads]
+ *   o_out    : bf16 [rows, num_heads, head_dim]; lse_out : fp32 [rows, num_heads] or NULL
+ *   head_dim : a power of two in [8, 256] (128 for MLA)
+ * O = (e^{la-m} Oa + e^{lb-m} Ob) / (e^{la-m} + e^{lb-m}), LSE = m + ln(...), m = max(la, lb);
+ * a side with LSE = -inf contributes nothing; both -inf gives O = 0, LSE = -inf.
+ * o_out may alias o_a (and lse_out lse_a): in-place accumulation is supported.
+ */
+MLA_API int mla_merge_state(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,
+                    void* o_out, float* lse_out, int64_t rows, int num_heads, int head_dim,
+                    void* stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+#endif /* MLA_PREFILL_H_ */

@@ -1,0 +1,108 @@
+"""GPU parity of the ragged prefill attention kernel against the fp64 oracle."""
+import numpy as np
+import pytest
+
+from chunked_prefill_attention_ragged_gb300 import workloads as wl
+from oracle import bf16_bits_to_f64, ragged_attention
+from gpu_util import bits_of, check_attention, f64_of_bf16, sample_rows, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+def run_gpu(b: wl.RaggedBatch, return_lse=True):
+    import chunked_prefill_attention_ragged_gb300 as mla
+    plan = mla.mla_prefill_plan(b.qo_indptr, b.kv_indptr, b.num_heads, causal=b.causal, sm_scale=b.sm_scale,
+                                window_left=b.window_left, logits_soft_cap=b.logits_soft_cap)
+    q, k, v = to_dev_bf16(b.q), to_dev_bf16(b.k), to_dev_bf16(b.v)
+    o, lse = plan.run(q, k, v, return_lse=return_lse)
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    return plan, (q, k, v), o, lse
+
+
+def oracle(b: wl.RaggedBatch, rows=None, heads=None):
+    return ragged_attention(b.q, b.k, b.v, b.qo_indptr, b.kv_indptr, causal=b.causal, sm_scale=b.sm_scale,
+                            window_left=b.window_left, logits_soft_cap=b.logits_soft_cap, rows=rows, heads=heads)
+
+
+SMALL = [
+    # name, q_lens, kv_lens, heads, causal, window, cap
+    ("tiny_workload", [17, 40], None, 4, True, -1, 0.0),
+    ("tile_edges", [1, 127, 128, 129, 255, 256, 257], None, 2, True, -1, 0.0),
+    ("prefix_longer_kv", [130, 7], [700, 300], 2, True, -1, 0.0),
+    ("fewer_keys_than_queries", [300, 200], [100, 50], 2, True, -1, 0.0),
+    ("noncausal_ragged", [300, 1, 77], [1000, 129, 5], 2, False, -1, 0.0),
+    ("empty_requests", [0, 45, 0, 130], [0, 45, 9, 130], 2, True, -1, 0.0),
+    ("noncausal_no_keys", [33, 20], [0, 64], 2, False, -1, 0.0),
+    ("window_100", [520, 130], None, 2, True, 100, 0.0),
+    ("window_0", [200], None, 1, True, 0, 0.0),
+    ("softcap_30", [260, 33], None, 2, True, -1, 30.0),
+    ("softcap_noncausal", [100], [300], 2, False, -1, 5.0),
+]
+
+
+@pytest.mark.parametrize("name,qlens,kvlens,heads,causal,window,cap", SMALL, ids=[c[0] for c in SMALL])
+def test_small_cases_full(name, qlens, kvlens, heads, causal, window, cap):
+    b = wl.random_ragged(100 + [c[0] for c in SMALL].index(name), qlens, kvlens, heads, causal=causal, window_left=window,
+                         logits_soft_cap=cap)
+    _, _, o, lse = run_gpu(b)
+    o_ref, lse_ref = oracle(b)
+    check_attention(f64_of_bf16(o), lse.double().cpu().numpy(), o_ref, lse_ref, name)
+
+
+def test_workload0_and_first_row_exact():
+    b = wl.make_workload(0)
+    _, _, o, lse = run_gpu(b)
+    o_ref, lse_ref = oracle(b)
+    check_attention(f64_of_bf16(o), lse.double().cpu().numpy(), o_ref, lse_ref, "workload0")
+    # Row 0 of each causal request sees only key 0: O is V[0] bit for bit.
+    ob = bits_of(o)
+    for r in range(b.batch):
+        s = b.qo_indptr[r]
+        np.testing.assert_array_equal(ob[s], b.v[b.kv_indptr[r]])
+
+
+def test_constant_v_and_lse_optional():
+    b = wl.random_ragged(5, [300, 129], None, 2)
+    c = wl.to_bf16_bits(np.random.default_rng(2).standard_normal(128).astype(np.float32))
+    b.v[:] = c[None, None, :]
+    _, _, o, lse = run_gpu(b, return_lse=False)
+    assert lse is None
+    np.testing.assert_allclose(f64_of_bf16(o), np.broadcast_to(bf16_bits_to_f64(c), o.shape), rtol=0, atol=1e-2)
+
+
+def test_repeat_runs_bitwise_identical():
+    b = wl.random_ragged(9, [700, 260, 3], None, 4)
+    plan, (q, k, v), o1, l1 = run_gpu(b)
+    o2, l2 = plan.run(q, k, v)
+    torch.cuda.synchronize()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("cap", [0.0, 30.0])
+def test_workload4_many_short_full(cap):
+    b = wl.make_workload(4, logits_soft_cap=cap)
+    _, _, o, lse = run_gpu(b)
+    o_ref, lse_ref = oracle(b)
+    check_attention(f64_of_bf16(o), lse.double().cpu().numpy(), o_ref, lse_ref, f"workload4 cap={cap}")
+
+
+def test_workload1_sampled_heads():
+    b = wl.make_workload(1)
+    _, _, o, lse = run_gpu(b)
+    heads = [0, 37, 77, 127]
+    o_ref, lse_ref = oracle(b, heads=heads)
+    check_attention(f64_of_bf16(o[:, heads]), lse[:, heads].double().cpu().numpy(), o_ref, lse_ref, "workload1")
+
+
+def test_workload3_long_sampled():
+    b = wl.make_workload(3)
+    _, _, o, lse = run_gpu(b)
+    rows = sample_rows(b.q_lens, n_random=64, every_tile=8, seed=3)
+    heads = [0, 64, 127]
+    o_ref, lse_ref = oracle(b, rows=rows, heads=heads)
+    idx = torch.from_numpy(np.concatenate([b.qo_indptr[r] + rows[r] for r in range(b.batch)])).cuda()
+    check_attention(f64_of_bf16(o[idx][:, heads]), lse[idx][:, heads].double().cpu().numpy(), o_ref, lse_ref,
+                    "workload3")

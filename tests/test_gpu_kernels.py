@@ -1,0 +1,132 @@
+"""GPU parity of the gather, up-projection and merge kernels against the oracle."""
+import numpy as np
+import pytest
+
+from chunked_prefill_attention_ragged_gb300 import workloads as wl
+from oracle import bf16_bits_to_f64, gather_latent, merge_state, round_f64_to_bf16, up_project
+from gpu_util import bits_of, f64_of_bf16, to_dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+def _mla():
+    import chunked_prefill_attention_ragged_gb300 as mla
+    return mla
+
+
+# ------------------------------------------------------------------ gather
+def test_gather_workload2_bit_exact():
+    mla = _mla()
+    cb = wl.make_chunked_prefix()
+    cache = to_dev_bf16(cb.cache)
+    table = to_dev(cb.block_table)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for c in range(cb.layout.num_chunks):
+        cu, st = cb.layout.cu_seq_lens[c], cb.layout.chunk_starts[c]
+        out = mla.mla_gather_latent(cache, table, to_dev(cu), to_dev(st), int(cu[-1]), status=status)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(bits_of(out), gather_latent(cb.cache, cb.block_table, cu, st))
+    assert int(status.item()) == 0
+
+
+@pytest.mark.parametrize("block_size,chunk", [(1, 3), (16, 40), (64, 100), (64, 4096)])
+def test_gather_random_tables(block_size, chunk):
+    mla = _mla()
+    cb = wl.random_chunked_prefix(block_size + chunk, [3, 3, 3], [0, 1000, 333], 1,
+                                  num_blocks=(2000 // block_size) + 8, block_size=block_size, chunk_tokens=chunk)
+    cache, table = to_dev_bf16(cb.cache), to_dev(cb.block_table)
+    for c in range(cb.layout.num_chunks):
+        cu, st = cb.layout.cu_seq_lens[c], cb.layout.chunk_starts[c]
+        out = mla.mla_gather_latent(cache, table, to_dev(cu), to_dev(st), int(cu[-1]))
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(bits_of(out), gather_latent(cb.cache, cb.block_table, cu, st))
+
+
+def test_gather_bad_block_id_flags_and_zeroes():
+    mla = _mla()
+    cb = wl.random_chunked_prefix(4, [2, 2], [70, 70], 1, num_blocks=4, block_size=64, chunk_tokens=128)
+    table = cb.block_table.copy()
+    table[1, 1] = 99                     # outside the cache
+    cu, st = cb.layout.cu_seq_lens[0], cb.layout.chunk_starts[0]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = mla.mla_gather_latent(to_dev_bf16(cb.cache), to_dev(table), to_dev(cu), to_dev(st), int(cu[-1]),
+                                status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 2
+    got = bits_of(out)
+    good = table.copy()
+    good[1, 1] = cb.block_table[1, 1]
+    ref = gather_latent(cb.cache, good, cu, st)
+    bad_rows = np.arange(cu[1] + 64, cu[2])     # request 1, positions 64..69
+    np.testing.assert_array_equal(got[bad_rows], 0)
+    keep = np.setdiff1d(np.arange(cu[-1]), bad_rows)
+    np.testing.assert_array_equal(got[keep], ref[keep])
+
+
+# ------------------------------------------------------------------ up-projection
+@pytest.mark.parametrize("tokens,heads", [(300, 4), (128, 1), (1, 2), (1000, 16)])
+def test_up_proj_matches_rounded_oracle(tokens, heads):
+    mla = _mla()
+    rng = np.random.default_rng(tokens + heads)
+    lat = wl.to_bf16_bits(rng.standard_normal((tokens, 576)).astype(np.float32))
+    w = wl.to_bf16_bits((rng.standard_normal((512, heads * 256)) * 512 ** -0.5).astype(np.float32))
+    k, v = mla.mla_up_proj(to_dev_bf16(lat), to_dev_bf16(w), heads)
+    torch.cuda.synchronize()
+    k_ref, v_ref = up_project(lat, w, heads)
+    kg, vg = f64_of_bf16(k), f64_of_bf16(v)
+    # rope part is a copy: bit-exact
+    np.testing.assert_array_equal(kg[:, :, 128:], k_ref[:, :, 128:])
+    for got, ref in ((kg[:, :, :128], k_ref[:, :, :128]), (vg, v_ref)):
+        rref = round_f64_to_bf16(ref)
+        mag = np.maximum(np.abs(ref), 2.0 ** -126)
+        ulp = 2.0 ** (np.floor(np.log2(mag)) - 7)          # bf16 spacing at the exact value
+        # fp32 accumulation may land one bf16 step away from the exact sum's rounding
+        assert np.all(np.abs(got - rref) <= ulp * 1.001)
+        assert np.mean(got != rref) < 0.01
+        assert np.abs(got - ref).max() <= 0.02
+
+
+# ------------------------------------------------------------------ merge
+def _merge_inputs(rows, heads, seed, dim=128):
+    rng = np.random.default_rng(seed)
+    oa = wl.to_bf16_bits(rng.standard_normal((rows, heads, dim)).astype(np.float32))
+    ob = wl.to_bf16_bits(rng.standard_normal((rows, heads, dim)).astype(np.float32))
+    la = (rng.standard_normal((rows, heads)) * 4).astype(np.float32)
+    lb = (rng.standard_normal((rows, heads)) * 4).astype(np.float32)
+    la[::7, 0] = -np.inf
+    lb[::5, -1] = -np.inf
+    la[3, :] = -np.inf
+    lb[3, :] = -np.inf
+    la[4, :] = 80.0
+    lb[4, :] = -80.0
+    return oa, la, ob, lb
+
+
+@pytest.mark.parametrize("rows,heads,dim", [(1000, 8, 128), (37, 128, 128), (64, 3, 64), (5, 2, 256)])
+def test_merge_matches_oracle(rows, heads, dim):
+    mla = _mla()
+    oa, la, ob, lb = _merge_inputs(rows, heads, rows, dim)
+    o, l = mla.mla_merge_state(to_dev_bf16(oa), to_dev(la), to_dev_bf16(ob), to_dev(lb))
+    torch.cuda.synchronize()
+    o_ref, l_ref = merge_state(oa, la.astype(np.float64), ob, lb.astype(np.float64))
+    og = f64_of_bf16(o)
+    assert np.abs(og - o_ref).max() <= 2.0 ** -8 * np.abs(o_ref).max() + 1e-6
+    lg = l.double().cpu().numpy()
+    assert np.array_equal(np.isneginf(lg), np.isneginf(l_ref))
+    fin = np.isfinite(l_ref)
+    assert np.abs(lg[fin] - l_ref[fin]).max() <= 1e-5 * max(1.0, np.abs(l_ref[fin]).max())
+    # one side empty: the other side is copied bit for bit
+    only_b = np.isneginf(la) & np.isfinite(lb)
+    np.testing.assert_array_equal(bits_of(o)[only_b], ob[only_b])
+
+
+def test_merge_in_place():
+    mla = _mla()
+    oa, la, ob, lb = _merge_inputs(500, 16, 11)
+    ta, tla = to_dev_bf16(oa), to_dev(la)
+    o_sep, l_sep = mla.mla_merge_state(ta.clone(), tla.clone(), to_dev_bf16(ob), to_dev(lb))
+    mla.mla_merge_state(ta, tla, to_dev_bf16(ob), to_dev(lb), ta, tla)
+    torch.cuda.synchronize()
+    assert torch.equal(ta.view(torch.int16), o_sep.view(torch.int16))
+    assert torch.equal(tla, l_sep)
