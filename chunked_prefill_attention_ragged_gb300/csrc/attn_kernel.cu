@@ -12,10 +12,11 @@
 //   warp 1      MMA issuer (one thread): S = Q K^T into one of two TMEM S buffers
 //               (tcgen05.mma, both operands from shared memory), then O += P V with P
 //               read from TMEM (written there by the softmax warps over the S buffer).
-//   warps 2-5   softmax: one thread per query row (= one TMEM lane).  Online softmax
-//               in base 2; O in TMEM is rescaled only when the running max grows by
-//               more than 2^8, so most tiles need no correction pass.  Epilogue
-//               normalises O, writes it (bf16) and the natural-log LSE (fp32).
+//   warps 2-9   softmax: two threads per query row (= one TMEM lane), each owning 64
+//               of the tile's 128 key columns and 64 of O's 128 columns.  Online
+//               softmax in base 2; O in TMEM is rescaled only when the running max
+//               grows by more than 2^8, so most tiles need no correction pass.
+//               Epilogue normalises O, writes it (bf16) and the natural-log LSE (fp32).
 // Every pipeline wait is bounded: on time-out the CTA records MLA_DEVSTAT_TIMEOUT,
 // drains its own copies and MMAs, frees TMEM and returns.
 #include <cuda_bf16.h>
@@ -38,11 +39,13 @@ constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + Q_PANELS * PANEL;
 constexpr int OFF_V = OFF_K + NSTAGE * K_PANELS * PANEL;
 constexpr int OFF_BAR = OFF_V + NSTAGE * V_PANELS * PANEL;
-enum Bar { QF = 0, QE = 1, KF = 2, KE = 4, VF = 6, VE = 8, SF = 10, PF = 12, OD = 14, FIN = 15, NBAR = 16 };
-constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+enum Bar { QF = 0, QE = 1, KF = 2, KE = 4, VF = 6, VE = 8, SF = 10, PF = 12, OD = 14, FIN = 15, XM = 16, XL = 18,
+           NBAR = 19 };
+constexpr int OFF_XCHG = OFF_BAR + NBAR * 8;      // row-max / row-sum exchange, 6 x 128 floats
+constexpr int OFF_MISC = OFF_XCHG + 6 * 128 * 4;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + slack for 1024-byte alignment
 
-constexpr int NTHREADS = 192;
+constexpr int NTHREADS = 320;                       // producer, MMA, 8 softmax warps
 constexpr uint32_t TMEM_COLS = 512;
 __device__ __forceinline__ constexpr uint32_t TM_S(int b) { return b ? 128u : 0u; }
 constexpr uint32_t TM_O = 256;
@@ -174,14 +177,24 @@ __device__ void run_mma(const Ctx& c, const PrefillParams& p, uint32_t tmem, int
 }
 
 // ------------------------------------------------------------------ softmax
-__device__ void run_softmax(const Ctx& c, const PrefillParams& p, uint32_t tmem, int ubeg, int uend) {
+// Two threads per query row: warps 2-5 own key columns 0-63 of every tile, warps 6-9
+// columns 64-127 (a warp may only touch TMEM lanes 32*(warp%4)..+31, so both halves cover
+// all 128 rows).  The halves agree on the row max through shared memory once per tile,
+// and on the row sum once per unit; both exchanges sit behind mbarriers so every wait
+// stays bounded.
+__device__ void run_softmax(const Ctx& c, const PrefillParams& p, uint32_t tmem, float* xchg,
+                            int ubeg, int uend) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;                 // TMEM lanes this warp may touch
+  const int half = (warp - 2) >> 2;          // 0: key columns 0-63, 1: 64-127
   const int row = quad * 32 + lane;
   const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
-  int s_g = 0, od_g = 0;
+  float* xmax = xchg;                        // [2 parity][2 half][128 rows]
+  float* xsum = xchg + 4 * 128;              // [2 half][128 rows]
+  int s_g = 0, od_g = 0, xl_g = 0;
   bool ok = true;
   const float NEG_INF = -__int_as_float(0x7f800000);
+  const float2 sc2 = make_float2(p.has_cap ? 1.f : p.scale_log2, p.has_cap ? 1.f : p.scale_log2);
   for (int ui = ubeg; ui < uend && ok; ++ui) {
     const Unit u = load_unit(p.units, ui);
     const int lo = u.kv_tiles & 0xFFFF, hi = (u.kv_tiles >> 16) & 0xFFFF;
@@ -191,60 +204,68 @@ __device__ void run_softmax(const Ctx& c, const PrefillParams& p, uint32_t tmem,
     const size_t orow = (size_t)(u.q_row0 + row) * p.num_heads + u.head;
     if (n <= 0) {
       if (row_ok) {
-        uint4* dst = reinterpret_cast<uint4*>(p.o + orow * 128);
+        uint4* dst = reinterpret_cast<uint4*>(p.o + orow * 128 + half * 64);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) dst[i] = make_uint4(0, 0, 0, 0);
-        if (p.lse) p.lse[orow] = NEG_INF;
+        for (int i = 0; i < 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+        if (p.lse && half == 0) p.lse[orow] = NEG_INF;
       }
       continue;
     }
     // Per-row key window inside the request: allowed positions [klo, khi).
     const int khi = p.causal ? min(u.kv_len, qpos + u.diag + 1) : u.kv_len;
     const int klo = p.window_left >= 0 ? max(0, qpos + u.diag - p.window_left) : 0;
-    float m_used = NEG_INF, l = 0.f;
+    float m_used = NEG_INF, l = 0.f;          // running max (log2 units) and this half's sum
     for (int j = 0; j < n; ++j) {
       const int sg = s_g + j, b = sg & 1;
       if (!__all_sync(0xffffffffu, c.wait(SF + b, (sg >> 1) & 1))) { ok = false; break; }
       tc_fence_after();
-      uint32_t sr[128];
-      tmem_ld128_sync(lane_addr + TM_S(b), sr);
-      float* t = reinterpret_cast<float*>(sr);
-      if (p.has_cap) {
+      float sv[64];
+      tmem_ld64_sync(lane_addr + TM_S(b) + half * 64, reinterpret_cast<uint32_t*>(sv));
+      if (p.has_cap) {   // soft cap, already in log2 units afterwards
 #pragma unroll
-        for (int i = 0; i < 128; ++i) t[i] = p.cap_log2 * tanhf(t[i] * p.x_to_cap);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 128; ++i) t[i] *= p.scale_log2;
+        for (int i = 0; i < 64; ++i) sv[i] = p.cap_log2 * tanhf(sv[i] * p.x_to_cap);
       }
-      const int kp0 = (lo + j) * BN;
+      const int kp0 = (lo + j) * BN + half * 64;
       const int c_hi = khi - kp0, c_lo = klo - kp0;
-      if (c_hi < BN || c_lo > 0) {
+      if (c_hi < 64 || c_lo > 0) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if (i >= c_hi || i < c_lo) t[i] = NEG_INF;
+        for (int i = 0; i < 64; ++i)
+          if (i >= c_hi || i < c_lo) sv[i] = NEG_INF;
       }
-      float mx = t[0];
+      // Row max of this half (raw logits: sm_scale > 0 keeps the order), then of the row.
+      float mx[8];
 #pragma unroll
-      for (int i = 1; i < 128; ++i) mx = fmaxf(mx, t[i]);
+      for (int k = 0; k < 8; ++k)
+        mx[k] = fmax3(fmax3(sv[8 * k], sv[8 * k + 1], sv[8 * k + 2]), fmax3(sv[8 * k + 3], sv[8 * k + 4], sv[8 * k + 5]),
+                      fmaxf(sv[8 * k + 6], sv[8 * k + 7]));
+      float m_half = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+      xmax[((sg & 1) * 2 + half) * 128 + row] = m_half;
+      mbar_arrive(c.bar(XM + b));
+      if (!__all_sync(0xffffffffu, c.wait(XM + b, (sg >> 1) & 1))) { ok = false; break; }
+      const float m_raw = fmaxf(m_half, xmax[((sg & 1) * 2 + (half ^ 1)) * 128 + row]);
+      const float mt = m_raw * sc2.x;       // tile max in log2 units (-inf stays -inf)
       float m_new = m_used;
       bool rescale = false;
       if (j == 0) {
-        m_new = mx;
-      } else if (mx > m_used + RESCALE_THRESHOLD) {
-        m_new = mx;
+        m_new = mt;
+      } else if (mt > m_used + RESCALE_THRESHOLD) {
+        m_new = mt;
         rescale = true;
       }
       const float msub = (m_new == NEG_INF) ? 0.f : m_new;
-      float sum = 0.f;
-      uint32_t pr[64];
+      const float2 neg_m = make_float2(-msub, -msub);
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      uint32_t pr[32];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const float p0 = ex2_approx(t[2 * i] - msub);
-        const float p1 = ex2_approx(t[2 * i + 1] - msub);
-        sum += p0 + p1;
-        pr[i] = pack_bf16x2(p0, p1);
+      for (int i = 0; i < 32; ++i) {
+        const float2 a = ffma2(make_float2(sv[2 * i], sv[2 * i + 1]), sc2, neg_m);
+        const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+        acc[i & 3] = fadd2(acc[i & 3], e);
+        pr[i] = pack_bf16x2(e.x, e.y);
       }
-      tmem_st64_sync(lane_addr + TM_S(b), pr);
+      const float2 s01 = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+      const float sum = s01.x + s01.y;
+      tmem_st32_sync(lane_addr + TM_S(b) + half * 32, pr);
       float alpha = 1.f;
       if (j > 0) {
         // O must hold P_{j-1} V_{j-1} before it may be rescaled.
@@ -255,11 +276,16 @@ __device__ void run_softmax(const Ctx& c, const PrefillParams& p, uint32_t tmem,
         // tcgen05.ld/st are warp-collective (.sync.aligned): the whole warp rescales
         // its 32 rows together, rows that keep their max with alpha = 1.
         if (__any_sync(0xffffffffu, rescale)) {
-          uint32_t orr[128];
-          tmem_ld128_sync(lane_addr + TM_O, orr);
+          float ov[64];
+          tmem_ld64_sync(lane_addr + TM_O + half * 64, reinterpret_cast<uint32_t*>(ov));
+          const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-          for (int i = 0; i < 128; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-          tmem_st128_sync(lane_addr + TM_O, orr);
+          for (int i = 0; i < 32; ++i) {
+            const float2 r = fmul2(make_float2(ov[2 * i], ov[2 * i + 1]), a2);
+            ov[2 * i] = r.x;
+            ov[2 * i + 1] = r.y;
+          }
+          tmem_st64_sync(lane_addr + TM_O + half * 64, reinterpret_cast<uint32_t*>(ov));
         }
       }
       l = l * alpha + sum;
@@ -271,25 +297,30 @@ __device__ void run_softmax(const Ctx& c, const PrefillParams& p, uint32_t tmem,
     if (!__all_sync(0xffffffffu, c.wait(OD, od_g & 1))) { ok = false; break; }
     ++od_g;
     tc_fence_after();
-    uint32_t orr[128];
-    tmem_ld128_sync(lane_addr + TM_O, orr);
+    float ov[64];
+    tmem_ld64_sync(lane_addr + TM_O + half * 64, reinterpret_cast<uint32_t*>(ov));
     tc_fence_before();
+    xsum[half * 128 + row] = l;
+    mbar_arrive(c.bar(XL));
+    if (!__all_sync(0xffffffffu, c.wait(XL, xl_g & 1))) { ok = false; break; }
+    ++xl_g;
+    const float l_row = l + xsum[(half ^ 1) * 128 + row];
     if (row_ok) {
-      const bool empty = !(l > 0.f);
-      const float inv = empty ? 0.f : 1.f / l;
-      uint4* dst = reinterpret_cast<uint4*>(p.o + orow * 128);
+      const bool empty = !(l_row > 0.f);
+      const float inv = empty ? 0.f : 1.f / l_row;
+      uint4* dst = reinterpret_cast<uint4*>(p.o + orow * 128 + half * 64);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
+      for (int i = 0; i < 8; ++i) {
         uint4 w;
-        w.x = pack_bf16x2(__uint_as_float(orr[8 * i + 0]) * inv, __uint_as_float(orr[8 * i + 1]) * inv);
-        w.y = pack_bf16x2(__uint_as_float(orr[8 * i + 2]) * inv, __uint_as_float(orr[8 * i + 3]) * inv);
-        w.z = pack_bf16x2(__uint_as_float(orr[8 * i + 4]) * inv, __uint_as_float(orr[8 * i + 5]) * inv);
-        w.w = pack_bf16x2(__uint_as_float(orr[8 * i + 6]) * inv, __uint_as_float(orr[8 * i + 7]) * inv);
+        w.x = pack_bf16x2(ov[8 * i + 0] * inv, ov[8 * i + 1] * inv);
+        w.y = pack_bf16x2(ov[8 * i + 2] * inv, ov[8 * i + 3] * inv);
+        w.z = pack_bf16x2(ov[8 * i + 4] * inv, ov[8 * i + 5] * inv);
+        w.w = pack_bf16x2(ov[8 * i + 6] * inv, ov[8 * i + 7] * inv);
         dst[i] = w;
       }
-      if (p.lse) {
+      if (p.lse && half == 0) {
         float lg;
-        asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(l));
+        asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(l_row));
         p.lse[orow] = empty ? NEG_INF : (m_used + lg) * 0.6931471805599453f;
       }
     }
@@ -309,8 +340,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBAR; ++i) mbar_init(c.bar(i), 1);
-    mbar_init(c.bar(PF + 0), 128);
-    mbar_init(c.bar(PF + 1), 128);
+    const int softmax_bars[5] = {PF + 0, PF + 1, XM + 0, XM + 1, XL};
+    for (int i = 0; i < 5; ++i) mbar_init(c.bar(softmax_bars[i]), 256);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -334,7 +365,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   } else if (warp == 1) {
     if (lane == 0) run_mma(c, p, tmem, ubeg, uend);
   } else {
-    run_softmax(c, p, tmem, ubeg, uend);
+    run_softmax(c, p, tmem, reinterpret_cast<float*>(smem + OFF_XCHG), ubeg, uend);
   }
   tc_fence_before();
   __syncthreads();

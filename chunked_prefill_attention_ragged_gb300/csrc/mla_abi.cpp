@@ -70,7 +70,8 @@ int mla_prefill_plan(mla_plan_t* out, const int32_t* qo_indptr, const int32_t* k
   *out = nullptr;
   if (!qo_indptr || !kv_indptr || batch < 0 || num_heads < 1 || num_heads > 65535) return MLA_ERR_INVALID_ARG;
   if (head_dim_qk != 192 || head_dim_vo != 128) return MLA_ERR_UNSUPPORTED;
-  if (!std::isfinite(sm_scale) || !std::isfinite(logits_soft_cap) || window_left < -1) return MLA_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale) || !(sm_scale > 0.f) || !std::isfinite(logits_soft_cap) || window_left < -1)
+    return MLA_ERR_INVALID_ARG;
   // Shape checks first (host only), so a bad call never touches the device.
   {
     PlanResult probe;

@@ -87,7 +87,7 @@ typedef struct mla_plan* mla_plan_t;
  *   head_dim_vo          : must be 128, else MLA_ERR_UNSUPPORTED.
  *   causal               : nonzero = causal, aligned bottom-right (query row i
  *       of a request sits at key position i + Lkv - Lq).
- *   sm_scale             : logits are sm_scale * q.k (finite, required).
+ *   sm_scale             : logits are sm_scale * q.k (finite and > 0, required).
  *   window_left          : -1 = none; w >= 0 keeps keys with position
  *       >= i + Lkv - Lq - w.  Values below -1 are invalid.
  *   logits_soft_cap      : <= 0 = none; c > 0 replaces a logit x by

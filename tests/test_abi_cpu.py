@@ -52,6 +52,8 @@ def test_plan_rejects_bad_arguments_without_touching_the_device():
     assert _plan_rc([0, 5], [0, 5], heads=0) == -1
     assert _plan_rc([0, 5], [0, 5], window=-2) == -1
     assert _plan_rc([0, 5], [0, 5], scale=float("nan")) == -1
+    assert _plan_rc([0, 5], [0, 5], scale=0.0) == -1
+    assert _plan_rc([0, 5], [0, 5], scale=-0.5) == -1
     assert _plan_rc([0, 5], [0, 5], cap=float("inf")) == -1
     assert _plan_rc([0, 5], [0, 5], batch=-1) == -1
 
