@@ -38,6 +38,8 @@ _SIGNATURES = {
                                    _c_vp, _c_vp, _c_vp]),
     "mla_up_proj": (_c_int, [_c_vp, _c_vp, _c_i64, _c_int, _c_vp, _c_vp, _c_vp, _c_vp]),
     "mla_merge_state": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_int, _c_int, _c_vp]),
+    "mla_prefill_run_noalloc": (_c_int, [_i32p, _i32p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_f, _c_int, _c_f,
+                                         _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
 }
 EXPORTED = tuple(_SIGNATURES)
 
@@ -263,3 +265,21 @@ def mla_merge_state(o_a, lse_a, o_b, lse_b, o_out=None, lse_out=None, stream=Non
                                      _dev(lse_out, f32, "lse_out"), rows, h, d, _stream(stream)),
            "mla_merge_state")
     return o_out, lse_out
+
+
+def mla_prefill_run_noalloc(qo_indptr, kv_indptr, num_heads: int, q, k, v, o, lse=None, *, causal: bool = True,
+                            sm_scale: float, window_left: int = -1, logits_soft_cap: float = 0.0, status=None,
+                            stream=None):
+    """Plan + run without any device allocation by the library (outputs are caller-provided).
+
+    For callers that cannot allocate device memory; the work list goes into a fixed
+    array inside the library, so overlapping calls must be serialised by the caller."""
+    import torch
+    qo, kv = _host_i32(qo_indptr), _host_i32(kv_indptr)
+    bf = torch.bfloat16
+    _check(library().mla_prefill_run_noalloc(
+        _ptr(qo), _ptr(kv), qo.size - 1, num_heads, 192, 128, int(bool(causal)), float(sm_scale), int(window_left),
+        float(logits_soft_cap), _dev(q, bf, "q"), _dev(k, bf, "k"), _dev(v, bf, "v"), _dev(o, bf, "o"),
+        _dev(lse, torch.float32, "lse"), _dev(status, torch.int32, "status"), _stream(stream)),
+        "mla_prefill_run_noalloc")
+    return o, lse

@@ -29,6 +29,7 @@ SOURCES = [
     "gather_kernel.cu",
     "merge_kernel.cu",
     "up_proj_kernel.cu",
+    "noalloc.cu",
 ]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

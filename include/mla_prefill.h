@@ -197,6 +197,38 @@ MLA_API int mla_merge_state(const void* o_a, const float* lse_a, const void* o_b
                     void* o_out, float* lse_out, int64_t rows, int num_heads, int head_dim,
                     void* stream);
 
+/* ======================================================================
+ * Allocation-free prefill (the pages have no counterpart; this exists for
+ * callers that cannot allocate device memory).
+ * ====================================================================== */
+/*
+ * Plan and run one ragged prefill in a single call without allocating device
+ * memory.  For callers that cannot call cudaMalloc: a serving engine whose
+ * memory pool already owns the device's HBM, a host that forbids allocation
+ * after start-up, or code that must not risk the synchronisation an
+ * allocation or free can bring.  Arguments are those of mla_prefill_plan
+ * followed by those of mla_prefill_run (same meaning, layout and checks),
+ * plus:
+ *   status : DEVICE int32 word or NULL.  When given, kernel-side problems are
+ *            OR-ed into it (MLA_DEVSTAT_*; the caller clears it); when NULL
+ *            they go to a word inside the library's scratch array that each
+ *            call clears and nobody reads.
+ * The work list lives in a fixed device array compiled into the library
+ * (about 2 MiB, held by every GPU that loads the library until exit).  Limit:
+ * at most 65536 work units, i.e. sum over requests of ceil(Lq / 128) times
+ * num_heads; larger problems return MLA_ERR_UNSUPPORTED before any device
+ * work.  The first call on a device looks the array's address up (once per
+ * device); make it before any stream capture.  Every call reuses the same
+ * array, so calls that overlap on the GPU (other streams, other host
+ * threads) race and must be serialised by the caller.  Planning happens on
+ * the host at every call.
+ */
+MLA_API int mla_prefill_run_noalloc(const int32_t* qo_indptr, const int32_t* kv_indptr, int batch,
+                                    int num_heads, int head_dim_qk, int head_dim_vo, int causal,
+                                    float sm_scale, int window_left, float logits_soft_cap,
+                                    const void* q, const void* k, const void* v, void* o, float* lse,
+                                    int32_t* status, void* stream);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif
