@@ -432,6 +432,22 @@ def bench_chunked(args, dev, peaks):
             acc["merge"].append(e3.elapsed_time(e4))
         total.append(evs[0].elapsed_time(marks[-1][4]))
     pipe.check_status()
+    # The gather alone, from a cold and clean L2: 256 MB written, then a second 256 MB
+    # buffer read, so no dirty line of earlier kernels is evicted inside the timed launch.
+    flush_read = torch.ones(64 << 20, dtype=torch.int32, device=dev)
+    t0 = int(pipe.chunk_tokens[0])
+    iso = []
+    for _ in range(10):
+        flush.zero_()
+        flush_read.sum()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        mla.mla_gather_latent(cache, table, pipe.cu_dev[0], pipe.starts_dev[0], t0, pipe.latent[:t0], pipe.status)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        iso.append(e0.elapsed_time(e1))
+    pipe.check_status()
+    del flush_read
     med = {n: statistics.median(x) for n, x in acc.items()}
     T = int(pipe.chunk_tokens[0])
     rows = b.q.shape[0]
@@ -457,6 +473,10 @@ def bench_chunked(args, dev, peaks):
                     "gbs": round(up_bytes / med["up_proj"] / 1e6, 1)},
         "gather": {"ms": round(med["gather"], 4), "gbs": round(gather_bytes / med["gather"] / 1e6, 1),
                    "frac_hbm": round(gather_bytes / med["gather"] / 1e6 / hbm, 3)},
+        "gather_isolated": {"ms": round(statistics.median(iso), 4),
+                            "gbs": round(gather_bytes / statistics.median(iso) / 1e6, 1),
+                            "frac_hbm": round(gather_bytes / statistics.median(iso) / 1e6 / hbm, 3),
+                            "l2": "256 MB written, then another 256 MB read, before each launch"},
         "merge": {"ms": round(med["merge"], 4), "gbs": round(merge_bytes / med["merge"] / 1e6, 1),
                   "frac_hbm": round(merge_bytes / med["merge"] / 1e6 / hbm, 3)},
         "hbm_peak_gbs": hbm, "hbm_peak_source": peaks["source"],

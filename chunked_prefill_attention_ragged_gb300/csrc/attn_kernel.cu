@@ -125,16 +125,19 @@ __device__ void run_producer(const Ctx& c, const PrefillParams& p, const CUtenso
 __device__ void run_mma(const Ctx& c, const PrefillParams& p, uint32_t tmem, int ubeg, int uend) {
   int q_g = 0, kv_g = 0, s_g = 0;
   bool ok = true;
+  const uint64_t q_desc = sdesc_sw128(c.sbase + OFF_Q, 16, 1024);
+  const uint64_t k_desc0 = sdesc_sw128(c.sbase + OFF_K, 16, 1024);
+  const uint64_t v_desc0 = sdesc_sw128(c.sbase + OFF_V, PANEL, 1024);
   auto issue_pv = [&](int t_local, int kv_base, int s_base) -> bool {
     const int sg = s_base + t_local, b = sg & 1;
     if (!c.wait(PF + b, (sg >> 1) & 1)) return false;
     const int g = kv_base + t_local, s = g % NSTAGE;
     if (!c.wait(VF + s, (g / NSTAGE) & 1)) return false;
     tc_fence_after();
-    const uint32_t vbase = c.sbase + OFF_V + s * V_PANELS * PANEL;
+    const uint64_t vd = v_desc0 + (uint64_t)(s * V_PANELS * PANEL >> 4);
 #pragma unroll
     for (int kk = 0; kk < BN / 16; ++kk) {
-      const uint64_t bd = sdesc_sw128(vbase + kk * 16 * 128, PANEL, 1024);
+      const uint64_t bd = vd + (uint64_t)(kk * 16 * 128 >> 4);
       mma_ts(tmem + TM_O, tmem + TM_S(b) + kk * 8, bd, IDESC_PV, (t_local > 0 || kk > 0) ? 1u : 0u);
     }
     tc_commit(c.bar(VE + s));
@@ -154,12 +157,12 @@ __device__ void run_mma(const Ctx& c, const PrefillParams& p, uint32_t tmem, int
       if (!c.wait(KF + s, (g / NSTAGE) & 1)) { ok = false; break; }
       tc_fence_after();
       const int b = (s_g + j) & 1;
-      const uint32_t kbase = c.sbase + OFF_K + s * K_PANELS * PANEL;
+      const uint64_t kd = k_desc0 + (uint64_t)(s * K_PANELS * PANEL >> 4);
 #pragma unroll
       for (int kk = 0; kk < 192 / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * PANEL + (kk & 3) * 32;
-        const uint64_t ad = sdesc_sw128(c.sbase + OFF_Q + off, 16, 1024);
-        const uint64_t bd = sdesc_sw128(kbase + off, 16, 1024);
+        const uint64_t off = (uint64_t)(((kk >> 2) * PANEL + (kk & 3) * 32) >> 4);
+        const uint64_t ad = q_desc + off;
+        const uint64_t bd = kd + off;
         mma_ss(tmem + TM_S(b), ad, bd, IDESC_QK, kk > 0 ? 1u : 0u);
       }
       tc_commit(c.bar(SF + b));
@@ -308,15 +311,20 @@ __device__ void run_softmax(const Ctx& c, const PrefillParams& p, uint32_t tmem,
     if (row_ok) {
       const bool empty = !(l_row > 0.f);
       const float inv = empty ? 0.f : 1.f / l_row;
-      uint4* dst = reinterpret_cast<uint4*>(p.o + orow * 128 + half * 64);
+      uint32_t w[32];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        uint4 w;
-        w.x = pack_bf16x2(ov[8 * i + 0] * inv, ov[8 * i + 1] * inv);
-        w.y = pack_bf16x2(ov[8 * i + 2] * inv, ov[8 * i + 3] * inv);
-        w.z = pack_bf16x2(ov[8 * i + 4] * inv, ov[8 * i + 5] * inv);
-        w.w = pack_bf16x2(ov[8 * i + 6] * inv, ov[8 * i + 7] * inv);
-        dst[i] = w;
+      for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(ov[2 * i] * inv, ov[2 * i + 1] * inv);
+      // This thread's 64 values are 128 contiguous bytes of its row.  Neighbouring lanes
+      // hold rows num_heads * 256 bytes apart, so each store instruction touches 32 rows:
+      // 32-byte stores write whole sectors and halve the instructions.
+      char* dstb = reinterpret_cast<char*>(p.o + orow * 128 + half * 64);
+      if (p.o_align32) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) st_global_v8(dstb + q * 32, w + 8 * q);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          reinterpret_cast<uint4*>(dstb)[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
       }
       if (p.lse && half == 0) {
         float lg;

@@ -3,10 +3,17 @@
 //
 // Slot rule from vLLM "vllm/models/deepseek_v4/sparse_mla.py",
 // _build_c128a_topk_metadata_kernel (decode branch): position p of request r lives in
-// block block_table[r, p / block_size] at offset p % block_size.  Rows are 16-byte
-// vectorised: consecutive threads copy consecutive 16-byte pieces of the output, so
-// stores are fully coalesced and each cache row is read as whole 128-byte lines.
+// block block_table[r, p / block_size] at offset p % block_size.
+//
+// Main kernel (rows up to 36 KB): one warp per CTA moves up to 32 consecutive output
+// rows.  Each lane resolves its row's cache slot and starts one bulk copy
+// (cp.async.bulk) of the whole row into shared memory; once all have landed, one bulk
+// copy writes the batch, which is contiguous in both shared and global memory, back
+// out.  Rows stay whole and 16-byte aligned end to end, and many CTAs per SM keep
+// enough bytes in flight to cover HBM latency.  Wider rows use the register-vector
+// kernel below.
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace mla {
 namespace {
@@ -72,6 +79,89 @@ gather_kernel(const uint4* __restrict__ cache, int64_t num_blocks, int block_siz
   }
 }
 
+constexpr int kBulkSmem = 36 * 1024;   // shared memory per bulk-gather CTA
+constexpr uint64_t kBulkWaitNs = 2000000000ull;
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(32)
+gather_bulk_kernel(const uint8_t* __restrict__ cache, int64_t num_blocks, int block_size, int row_bytes,
+                   int rows_per_cta, const int32_t* __restrict__ block_table, int max_blocks,
+                   const int32_t* __restrict__ cu, const int32_t* __restrict__ starts, int batch,
+                   int64_t total_rows, uint8_t* __restrict__ out, int32_t* status) {
+  extern __shared__ __align__(128) uint8_t rows_smem[];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  const int lane = threadIdx.x;
+  const int64_t row0 = (int64_t)blockIdx.x * rows_per_cta;
+  const int nrows = total_rows - row0 < rows_per_cta ? (int)(total_rows - row0) : rows_per_cta;
+  const uint32_t bar_a = smem_addr(&bar);
+  if (lane == 0) {
+    mbar_init(bar_a, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncwarp();
+  // Resolve this lane's row.  With at most 31 requests the warp loads cu and starts
+  // once (lane i holds cu[i] and starts[i]) and finds each row's request by shuffles,
+  // which leaves the block-table read as the only dependent load before the copy.
+  const int64_t row = row0 + lane;
+  bool active = lane < nrows, ok = false;
+  int64_t slot = 0;
+  int r = 0;
+  int64_t cu_r = 0, cu_r1 = 0, start_r = 0;
+  if (batch < 32) {
+    const int32_t cu_l = lane <= batch ? __ldg(cu + lane) : 0x7fffffff;
+    const int32_t st_l = lane < batch ? __ldg(starts + lane) : 0;
+    for (int i = 1; i < batch; ++i) r += __shfl_sync(0xffffffffu, cu_l, i) <= row ? 1 : 0;
+    cu_r = __shfl_sync(0xffffffffu, cu_l, r);
+    cu_r1 = __shfl_sync(0xffffffffu, cu_l, r + 1);
+    start_r = __shfl_sync(0xffffffffu, st_l, r);
+  } else if (active) {
+    r = find_request(cu, batch, row);
+    cu_r = __ldg(cu + r);
+    cu_r1 = __ldg(cu + r + 1);
+    start_r = __ldg(starts + r);
+  }
+  if (active) {
+    const int64_t t = row - cu_r;
+    const int64_t pos = start_r + t;
+    const int64_t bi = pos / block_size;
+    ok = row < cu_r1 && pos >= 0 && bi < max_blocks;
+    const int64_t blk = ok ? (int64_t)__ldg(block_table + (int64_t)r * max_blocks + bi) : -1;
+    ok = ok && blk >= 0 && blk < num_blocks;
+    slot = ok ? blk * block_size + (pos - bi * block_size) : 0;
+  }
+  const unsigned good = __ballot_sync(0xffffffffu, active && ok);
+  if (active && !ok) {   // unknown block: the row is written as zeros and flagged
+    uint4* z = reinterpret_cast<uint4*>(rows_smem + (size_t)lane * row_bytes);
+    for (int i = 0; i < row_bytes / 16; ++i) z[i] = make_uint4(0, 0, 0, 0);
+    if (status) atomicOr(status, MLA_DEVSTAT_BAD_INDEX);
+  }
+  // Generic-proxy zero rows must be visible to the bulk copy that reads them.
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
+  if (lane == 0) mbar_arrive_expect_tx(bar_a, (uint32_t)__popc(good) * (uint32_t)row_bytes);
+  __syncwarp();
+  if (active && ok)
+    bulk_g2s(smem_addr(rows_smem) + (uint32_t)lane * row_bytes, cache + slot * row_bytes, (uint32_t)row_bytes,
+             bar_a);
+  if (lane == 0) {
+    int dummy = 0;
+    if (mbar_wait_bounded(bar_a, 0, &abort_flag, status ? status : &dummy, MLA_DEVSTAT_TIMEOUT, kBulkWaitNs))
+      bulk_s2g(out + row0 * row_bytes, smem_addr(rows_smem), (uint32_t)nrows * (uint32_t)row_bytes);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_gather(const void* cache, int64_t num_blocks, int block_size, int entry_dim,
@@ -81,6 +171,17 @@ cudaError_t launch_gather(const void* cache, int64_t num_blocks, int block_size,
   const int vec_per_row = entry_dim * 2 / 16;
   const int64_t total_vec = total_tokens * vec_per_row;
   if (total_vec == 0) return cudaSuccess;
+  const int row_bytes = entry_dim * 2;
+  if (row_bytes <= kBulkSmem) {
+    const int rows_per_cta = min(32, kBulkSmem / row_bytes);
+    const int64_t grid = (total_tokens + rows_per_cta - 1) / rows_per_cta;
+    if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+    const int smem = rows_per_cta * row_bytes;
+    gather_bulk_kernel<<<(unsigned)grid, 32, smem, stream>>>(
+        static_cast<const uint8_t*>(cache), num_blocks, block_size, row_bytes, rows_per_cta, block_table,
+        max_blocks_per_req, cu_seq_lens, chunk_starts, batch, total_tokens, static_cast<uint8_t*>(out), status);
+    return cudaGetLastError();
+  }
   const int sms = device_sm_count();
   const int64_t want = (total_vec + (int64_t)kThreads * kVecPerThread - 1) / ((int64_t)kThreads * kVecPerThread);
   const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 8;

@@ -18,6 +18,7 @@ struct PrefillParams {
   __nv_bfloat16* o;           // [total_q, H, 128]
   float* lse;                 // [total_q, H] or null
   int num_heads;
+  int o_align32;              // o is 32-byte aligned: the epilogue uses 32-byte stores
   int causal;
   int window_left;
   int has_cap;

@@ -161,6 +161,7 @@ int mla_prefill_run(mla_plan_t p, const void* q, const void* k, const void* v, v
   prm.cta_offsets = p->d_offsets;
   prm.status = p->d_status;
   prm.o = static_cast<__nv_bfloat16*>(o);
+  prm.o_align32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
   prm.lse = lse;
   prm.num_heads = p->num_heads;
   prm.causal = p->causal;

@@ -121,6 +121,7 @@ extern "C" MLA_API int mla_prefill_run_noalloc(const int32_t* qo_indptr, const i
   prm.cta_offsets = d_offsets;
   prm.status = d_status;
   prm.o = static_cast<__nv_bfloat16*>(o);
+  prm.o_align32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
   prm.lse = lse;
   prm.num_heads = num_heads;
   prm.causal = causal != 0;

@@ -39,6 +39,10 @@ SMALL = [
     ("window_0", [200], None, 1, True, 0, 0.0),
     ("softcap_30", [260, 33], None, 2, True, -1, 30.0),
     ("softcap_noncausal", [100], [300], 2, False, -1, 5.0),
+    ("block_edges", [383, 384, 385, 511, 512, 513], None, 2, True, -1, 0.0),
+    ("ring_wrap_noncausal", [300, 40], [2000, 1500], 2, False, -1, 0.0),
+    ("window_300_long", [1500], None, 1, True, 300, 0.0),
+    ("prefix_window", [260], [1000], 2, True, 200, 0.0),
 ]
 
 
@@ -70,6 +74,22 @@ def test_constant_v_and_lse_optional():
     _, _, o, lse = run_gpu(b, return_lse=False)
     assert lse is None
     np.testing.assert_allclose(f64_of_bf16(o), np.broadcast_to(bf16_bits_to_f64(c), o.shape), rtol=0, atol=1e-2)
+
+
+def test_output_alignment_paths_agree():
+    # A 32-byte aligned O takes 32-byte stores, a 16-byte aligned one 16-byte stores.
+    import chunked_prefill_attention_ragged_gb300 as mla
+    b = wl.random_ragged(31, [300, 129], None, 4)
+    plan = mla.mla_prefill_plan(b.qo_indptr, b.kv_indptr, b.num_heads, causal=True, sm_scale=b.sm_scale)
+    q, k, v = to_dev_bf16(b.q), to_dev_bf16(b.k), to_dev_bf16(b.v)
+    rows = b.q.shape[0]
+    o32, lse32 = plan.run(q, k, v)
+    buf = torch.zeros(rows * 4 * 128 + 8, dtype=torch.bfloat16, device="cuda")
+    o16 = buf[8:].view(rows, 4, 128)
+    assert o16.data_ptr() % 32 == 16
+    plan.run(q, k, v, o=o16, lse=torch.empty_like(lse32))
+    torch.cuda.synchronize()
+    assert torch.equal(o32.view(torch.int16), o16.view(torch.int16))
 
 
 def test_repeat_runs_bitwise_identical():

@@ -64,6 +64,22 @@ def test_gather_bad_block_id_flags_and_zeroes():
     np.testing.assert_array_equal(got[keep], ref[keep])
 
 
+@pytest.mark.parametrize("entry_dim", [8, 72, 18432, 18440])
+def test_gather_row_widths(entry_dim):
+    # 16-byte rows up to 36 KB go through the bulk-copy kernel (several rows per CTA,
+    # partial last batch); wider rows take the register-vector kernel.
+    mla = _mla()
+    rng = np.random.default_rng(entry_dim)
+    num_blocks, block_size = 7, 4
+    cache = rng.integers(0, 1 << 16, size=(num_blocks, block_size, entry_dim), dtype=np.uint16)
+    table = rng.permutation(num_blocks)[:6].reshape(2, 3).astype(np.int32)
+    cu = np.array([0, 9, 19], dtype=np.int32)
+    st = np.array([1, 0], dtype=np.int32)
+    out = mla.mla_gather_latent(to_dev_bf16(cache), to_dev(table), to_dev(cu), to_dev(st), int(cu[-1]))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(bits_of(out), gather_latent(cache, table, cu, st))
+
+
 # ------------------------------------------------------------------ up-projection
 @pytest.mark.parametrize("tokens,heads", [(300, 4), (128, 1), (1, 2), (1000, 16)])
 def test_up_proj_matches_rounded_oracle(tokens, heads):
