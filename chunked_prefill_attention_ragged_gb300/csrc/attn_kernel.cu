@@ -7,8 +7,8 @@
 // logits_soft_cap; FlashInferPrefillImpl.run_prefill_*: O and LSE per (row, head)).
 //
 // Design (one persistent CTA per SM, one work unit = 128 query rows of one head):
-//   warp 0      TMA producer: Q tile once per unit, then K and V tiles of 128 keys
-//               through two-stage rings (K and V released separately).
+//   warps 0, 10 TMA producers: warp 0 loads the Q tile once per unit and K tiles of 128
+//               keys, warp 10 V tiles, each through a two-stage ring.
 //   warp 1      MMA issuer (one thread): S = Q K^T into one of two TMEM S buffers
 //               (tcgen05.mma, both operands from shared memory), then O += P V with P
 //               read from TMEM (written there by the softmax warps over the S buffer).
@@ -39,13 +39,22 @@ constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + Q_PANELS * PANEL;
 constexpr int OFF_V = OFF_K + NSTAGE * K_PANELS * PANEL;
 constexpr int OFF_BAR = OFF_V + NSTAGE * V_PANELS * PANEL;
-enum Bar { QF = 0, QE = 1, KF = 2, KE = 4, VF = 6, VE = 8, SF = 10, PF = 12, OD = 14, FIN = 15, XM = 16, XL = 18,
-           NBAR = 19 };
+enum Bar {
+  QF = 0, QE = 1,       // Q landed / released
+  KF = 2, KE = 4,       // [stage] K tile landed / released
+  PV = 6,               // [tile parity] V tile landed AND P written by all 8 softmax warps
+  VE = 8,               // [stage] V tile released
+  SF = 10,              // [S buffer] S = Q K^T done
+  OD = 12,              // O += P V done
+  FIN = 13,             // all MMAs drained before TMEM is released
+  XM = 14, XL = 16,     // softmax half-row exchanges (max per tile, sum per unit)
+  NBAR = 17
+};
 constexpr int OFF_XCHG = OFF_BAR + NBAR * 8;      // row-max / row-sum exchange, 6 x 128 floats
 constexpr int OFF_MISC = OFF_XCHG + 6 * 128 * 4;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + slack for 1024-byte alignment
 
-constexpr int NTHREADS = 320;                       // producer, MMA, 8 softmax warps
+constexpr int NTHREADS = 352;                       // Q/K producer, MMA, 8 softmax warps, V producer
 constexpr uint32_t TMEM_COLS = 512;
 __device__ __forceinline__ constexpr uint32_t TM_S(int b) { return b ? 128u : 0u; }
 constexpr uint32_t TM_O = 256;
@@ -80,10 +89,15 @@ __device__ __forceinline__ Unit load_unit(const Unit* units, int i) {
   return u;
 }
 
-// ------------------------------------------------------------------ producer
-__device__ void run_producer(const Ctx& c, const PrefillParams& p, const CUtensorMap* tq,
-                             const CUtensorMap* tk, const CUtensorMap* tv, int ubeg, int uend) {
-  int q_g = 0, k_g = 0, v_g = 0;   // loads issued so far (Q tiles, K tiles, V tiles)
+// ------------------------------------------------------------------ producers
+// Two producer threads, so that a K load never queues behind a V load waiting for its
+// stage: warp 0 loads Q (once per unit) and K tiles, warp 10 loads V tiles.  A K stage
+// frees when its S = Q K^T is done, a V stage when its P V is done.  A V load lands on
+// the tile's PV barrier, which also counts the softmax warps' P arrivals, so the MMA
+// issuer waits once for both inputs of P V.
+__device__ void run_producer_qk(const Ctx& c, const PrefillParams& p, const CUtensorMap* tq,
+                                const CUtensorMap* tk, int ubeg, int uend) {
+  int q_g = 0, k_g = 0;   // loads issued so far (Q tiles, K tiles)
   bool ok = true;
   for (int ui = ubeg; ui < uend && ok; ++ui) {
     const Unit u = load_unit(p.units, ui);
@@ -96,29 +110,44 @@ __device__ void run_producer(const Ctx& c, const PrefillParams& p, const CUtenso
     ++q_g;
     for (int t = lo; t < hi; ++t) {
       const int row = u.kv_row0 + t * BN;
-      int s = k_g % NSTAGE;
-      uint32_t use = k_g / NSTAGE;
+      const int s = k_g % NSTAGE;
+      const uint32_t use = k_g / NSTAGE;
       if (use > 0 && !c.wait(KE + s, (use - 1) & 1)) { ok = false; break; }
       mbar_arrive_expect_tx(c.bar(KF + s), K_PANELS * PANEL);
       for (int i = 0; i < K_PANELS; ++i)
         tma_load_3d(c.sbase + OFF_K + (s * K_PANELS + i) * PANEL, tk, c.bar(KF + s), i * 64, u.head, row);
       ++k_g;
-      s = v_g % NSTAGE;
-      use = v_g / NSTAGE;
-      if (use > 0 && !c.wait(VE + s, (use - 1) & 1)) { ok = false; break; }
-      mbar_arrive_expect_tx(c.bar(VF + s), V_PANELS * PANEL);
-      for (int i = 0; i < V_PANELS; ++i)
-        tma_load_3d(c.sbase + OFF_V + (s * V_PANELS + i) * PANEL, tv, c.bar(VF + s), i * 64, u.head, row);
-      ++v_g;
     }
   }
   // Let every copy this thread started land before the CTA can exit: wait for the
   // last phase issued on each barrier (already complete on the normal path).
   if (q_g > 0) c.drain(QF, (q_g - 1) & 1);
-  for (int s = 0; s < NSTAGE; ++s) {
+  for (int s = 0; s < NSTAGE; ++s)
     if (k_g > s) c.drain(KF + s, (((k_g - 1 - s) / NSTAGE)) & 1);
-    if (v_g > s) c.drain(VF + s, (((v_g - 1 - s) / NSTAGE)) & 1);
+}
+
+__device__ void run_producer_v(const Ctx& c, const PrefillParams& p, const CUtensorMap* tv, int ubeg,
+                               int uend) {
+  int v_g = 0;
+  bool ok = true;
+  for (int ui = ubeg; ui < uend && ok; ++ui) {
+    const Unit u = load_unit(p.units, ui);
+    const int lo = u.kv_tiles & 0xFFFF, hi = (u.kv_tiles >> 16) & 0xFFFF;
+    for (int t = lo; t < hi; ++t) {
+      const int row = u.kv_row0 + t * BN;
+      const int s = v_g % NSTAGE;
+      const uint32_t use = v_g / NSTAGE;
+      if (use > 0 && !c.wait(VE + s, (use - 1) & 1)) { ok = false; break; }
+      mbar_arrive_expect_tx(c.bar(PV + s), V_PANELS * PANEL);
+      for (int i = 0; i < V_PANELS; ++i)
+        tma_load_3d(c.sbase + OFF_V + (s * V_PANELS + i) * PANEL, tv, c.bar(PV + s), i * 64, u.head, row);
+      ++v_g;
+    }
   }
+  // The last phase of a PV barrier also needs the softmax warps' arrivals, which come on
+  // the normal path; after an abort this gives up at the drain limit.
+  for (int s = 0; s < NSTAGE; ++s)
+    if (v_g > s) c.drain(PV + s, (((v_g - 1 - s) / NSTAGE)) & 1);
 }
 
 // ------------------------------------------------------------------ MMA issuer
@@ -129,10 +158,11 @@ __device__ void run_mma(const Ctx& c, const PrefillParams& p, uint32_t tmem, int
   const uint64_t k_desc0 = sdesc_sw128(c.sbase + OFF_K, 16, 1024);
   const uint64_t v_desc0 = sdesc_sw128(c.sbase + OFF_V, PANEL, 1024);
   auto issue_pv = [&](int t_local, int kv_base, int s_base) -> bool {
+    // Tiles are counted alike for S buffers and V stages (both advance once per tile),
+    // so one barrier per parity covers "P written" and "V landed".
     const int sg = s_base + t_local, b = sg & 1;
-    if (!c.wait(PF + b, (sg >> 1) & 1)) return false;
     const int g = kv_base + t_local, s = g % NSTAGE;
-    if (!c.wait(VF + s, (g / NSTAGE) & 1)) return false;
+    if (!c.wait(PV + b, (sg >> 1) & 1)) return false;
     tc_fence_after();
     const uint64_t vd = v_desc0 + (uint64_t)(s * V_PANELS * PANEL >> 4);
 #pragma unroll
@@ -294,7 +324,8 @@ __device__ void run_softmax(const Ctx& c, const PrefillParams& p, uint32_t tmem,
       l = l * alpha + sum;
       m_used = m_new;
       tc_fence_before();
-      mbar_arrive(c.bar(PF + b));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(PV + b));
     }
     if (!ok) break;
     if (!__all_sync(0xffffffffu, c.wait(OD, od_g & 1))) { ok = false; break; }
@@ -348,8 +379,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBAR; ++i) mbar_init(c.bar(i), 1);
-    const int softmax_bars[5] = {PF + 0, PF + 1, XM + 0, XM + 1, XL};
-    for (int i = 0; i < 5; ++i) mbar_init(c.bar(softmax_bars[i]), 256);
+    const int softmax_bars[3] = {XM + 0, XM + 1, XL};
+    for (int i = 0; i < 3; ++i) mbar_init(c.bar(softmax_bars[i]), 256);
+    mbar_init(c.bar(PV + 0), 9);   // 8 softmax warps + the V producer's expect_tx arrival
+    mbar_init(c.bar(PV + 1), 9);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -369,9 +402,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   const int ubeg = p.cta_offsets[blockIdx.x], uend = p.cta_offsets[blockIdx.x + 1];
 
   if (warp == 0) {
-    if (lane == 0) run_producer(c, p, &tm_q, &tm_k, &tm_v, ubeg, uend);
+    if (lane == 0) run_producer_qk(c, p, &tm_q, &tm_k, ubeg, uend);
   } else if (warp == 1) {
     if (lane == 0) run_mma(c, p, tmem, ubeg, uend);
+  } else if (warp == 10) {
+    if (lane == 0) run_producer_v(c, p, &tm_v, ubeg, uend);
   } else {
     run_softmax(c, p, tmem, reinterpret_cast<float*>(smem + OFF_XCHG), ubeg, uend);
   }

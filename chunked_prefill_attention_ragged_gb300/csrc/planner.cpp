@@ -90,8 +90,9 @@ int build_plan(const int32_t* qo, const int32_t* kv, int batch, int num_heads, b
       u.kv_len = (int32_t)lkv;
       u.diag = (int32_t)diag;
       u.kv_tiles = tlo | (thi << 16);
-      // Cost in key-tile units plus a fixed share for loading Q and writing O.
-      tiles.push_back({u, (int64_t)(thi - tlo) + 1});
+      // Cost in half key tiles: two per key tile plus three for the unit's fixed work
+      // (Q load, pipeline fill, epilogue), which measures at about 1.5 key tiles.
+      tiles.push_back({u, 2 * (int64_t)(thi - tlo) + 3});
     }
     // Longest tiles first inside a group.
     std::stable_sort(tiles.begin(), tiles.end(),
@@ -105,7 +106,7 @@ int build_plan(const int32_t* qo, const int32_t* kv, int batch, int num_heads, b
         u.head = h;
         pending.push_back(u);
         pending_cost.push_back(t.second);
-        out->kv_tiles += t.second - 1;
+        out->kv_tiles += (t.second - 3) / 2;
       }
       groups.push_back(g);
     }
