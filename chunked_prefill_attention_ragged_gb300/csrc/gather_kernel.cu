@@ -5,13 +5,13 @@
 // _build_c128a_topk_metadata_kernel (decode branch): position p of request r lives in
 // block block_table[r, p / block_size] at offset p % block_size.
 //
-// Main kernel (rows up to 36 KB): one warp per CTA moves up to 32 consecutive output
-// rows.  Each lane resolves its row's cache slot and starts one bulk copy
-// (cp.async.bulk) of the whole row into shared memory; once all have landed, one bulk
-// copy writes the batch, which is contiguous in both shared and global memory, back
-// out.  Rows stay whole and 16-byte aligned end to end, and many CTAs per SM keep
-// enough bytes in flight to cover HBM latency.  Wider rows use the register-vector
-// kernel below.
+// Main kernel (rows up to 36 KB): one warp per CTA moves a batch of consecutive output
+// rows (about 4.5 KB: 4 rows of 576 bf16).  Each lane resolves its row's cache slot and
+// starts one bulk copy (cp.async.bulk) of the whole row into shared memory; once all
+// have landed, one bulk copy writes the batch, which is contiguous in both shared and
+// global memory, back out.  Small batches give many CTAs per SM, so loads of some
+// overlap stores of others; measured, this matches a plain device-to-device copy of
+// the same bytes.  Wider rows use the register-vector kernel below.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -79,7 +79,8 @@ gather_kernel(const uint4* __restrict__ cache, int64_t num_blocks, int block_siz
   }
 }
 
-constexpr int kBulkSmem = 36 * 1024;   // shared memory per bulk-gather CTA
+constexpr int kBulkBatch = 4608;        // bytes per bulk-gather CTA (4 rows of 576 bf16)
+constexpr int kBulkMaxRow = 36 * 1024;  // widest row the bulk path takes
 constexpr uint64_t kBulkWaitNs = 2000000000ull;
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -172,8 +173,8 @@ cudaError_t launch_gather(const void* cache, int64_t num_blocks, int block_size,
   const int64_t total_vec = total_tokens * vec_per_row;
   if (total_vec == 0) return cudaSuccess;
   const int row_bytes = entry_dim * 2;
-  if (row_bytes <= kBulkSmem) {
-    const int rows_per_cta = min(32, kBulkSmem / row_bytes);
+  if (row_bytes <= kBulkMaxRow) {
+    const int rows_per_cta = max(1, min(32, kBulkBatch / row_bytes));
     const int64_t grid = (total_tokens + rows_per_cta - 1) / rows_per_cta;
     if (grid > 0x7fffffff) return cudaErrorInvalidValue;
     const int smem = rows_per_cta * row_bytes;

@@ -7,14 +7,21 @@
 // 192-dim K and 128-dim V; this kernel is that decompression, with the rope copy fused
 // into the epilogue so K and V are written once, in their final layout.
 //
-// Persistent kernel, one CTA per SM, output tile = 128 tokens x one head (N = 256):
-//   warp 0     TMA producer: latent panel [128 x 64] (K-major) and W panel
-//              [64 x 256] (N-major) per 64-wide slice of the 512 reduction, 4-stage ring.
+// Persistent kernel, one CTA per SM, output tile = 128 tokens x one head (N = 256).
+// Each CTA takes a contiguous range of tiles ordered (token block, head) with the head
+// fastest, so the 128-token latent tile (A, 128 x 512, 128 KB) stays in shared memory
+// while the CTA walks through heads; only W's 512 x 256 slice of each head (B, 256 KB)
+// streams.  Per tile that is 256 KB of operand traffic for 4096 cycles of MMA instead
+// of 384 KB, below what L2 delivers to one SM.
+//   warp 0     TMA producer: the latent tile when the token block changes (8 K-major
+//              panels of 128 x 64), and W's slice as [64 x 256] blocks (4 N-major
+//              panels of 64 x 64) through a 3-stage ring.
 //   warp 1     MMA issuer: tcgen05.mma M=128 N=256 K=16 into one of two TMEM
 //              accumulators (512 columns), so the epilogue of tile i overlaps the
 //              MMAs of tile i+1.
 //   warps 2-5  epilogue: one thread per token row reads its accumulator row, rounds to
-//              bf16 and writes K_nope, V and the rope copy.
+//              bf16 and writes K_nope, V and the rope copy (read once per token block)
+//              with 32-byte stores when the outputs allow it.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -25,16 +32,18 @@ namespace mla {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64, KDIM = 512, KBLOCKS = KDIM / BK;
-constexpr int NS = 4;
-constexpr int A_BYTES = BM * BK * 2;          // 16 KB
+constexpr int NS = 3;
+constexpr int A_PANEL = BM * BK * 2;          // 16 KB: 128 token rows x 64 latent columns
+constexpr int A_BYTES = KBLOCKS * A_PANEL;    // 128 KB: the whole 128 x 512 latent tile
 constexpr int B_PANEL = BK * 64 * 2;          // 8 KB: 64 k-rows x 64 n
 constexpr int B_BYTES = 4 * B_PANEL;          // 32 KB
 constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + NS * A_BYTES;
+constexpr int OFF_B = OFF_A + A_BYTES;
 constexpr int OFF_BAR = OFF_B + NS * B_BYTES;
-enum Bar { FULL = 0, EMPTY = 4, AFULL = 8, AEMPTY = 10, FIN = 12, NBAR = 13 };
+enum Bar { FULL = 0, EMPTY = 3, AFULL = 6, AEMPTY = 8, LF = 10, LE = 11, FIN = 12, NBAR = 13 };
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 constexpr int NTHREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, false, true);
@@ -63,7 +72,13 @@ struct UpParams {
   int64_t num_tokens;
   int num_heads;
   int num_tiles;
+  int out_align32;   // k and v 32-byte aligned: 32-byte stores
 };
+
+__device__ __forceinline__ void tile_range(int num_tiles, int& beg, int& end) {
+  beg = (int)((int64_t)blockIdx.x * num_tiles / gridDim.x);
+  end = (int)((int64_t)(blockIdx.x + 1) * num_tiles / gridDim.x);
+}
 
 __global__ void __launch_bounds__(NTHREADS, 1)
 up_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
@@ -91,29 +106,46 @@ up_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  int tbeg, tend;
+  tile_range(p.num_tiles, tbeg, tend);
+  const int H = p.num_heads;
 
   if (warp == 0 && lane == 0) {
-    int it = 0;
+    int it = 0, a_loads = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x) {
-      const int m0 = (tile / p.num_heads) * BM, h = tile % p.num_heads;
+    for (int tile = tbeg; tile < tend && ok; ++tile) {
+      const int m = tile / H, h = tile % H;
+      if (tile == tbeg || h == 0) {   // new token block: reload the latent tile
+        if (a_loads > 0 && !c.wait(LE, (a_loads - 1) & 1)) { ok = false; break; }
+        mbar_arrive_expect_tx(c.bar(LF), A_BYTES);
+        for (int kb = 0; kb < KBLOCKS; ++kb)
+          tma_load_2d(c.sbase + OFF_A + kb * A_PANEL, &tm_a, c.bar(LF), kb * BK, m * BM);
+        ++a_loads;
+      }
       for (int kb = 0; kb < KBLOCKS; ++kb, ++it) {
         const int s = it % NS;
         const uint32_t use = it / NS;
         if (use > 0 && !c.wait(EMPTY + s, (use - 1) & 1)) { ok = false; break; }
-        mbar_arrive_expect_tx(c.bar(FULL + s), A_BYTES + B_BYTES);
-        tma_load_2d(c.sbase + OFF_A + s * A_BYTES, &tm_a, c.bar(FULL + s), kb * BK, m0);
+        mbar_arrive_expect_tx(c.bar(FULL + s), B_BYTES);
         for (int i = 0; i < 4; ++i)
           tma_load_2d(c.sbase + OFF_B + s * B_BYTES + i * B_PANEL, &tm_b, c.bar(FULL + s),
                       h * BN + i * 64, kb * BK);
       }
     }
+    if (a_loads > 0) c.drain(LF, (a_loads - 1) & 1);
     for (int s = 0; s < NS; ++s)
       if (it > s) c.drain(FULL + s, ((it - 1 - s) / NS) & 1);
   } else if (warp == 1 && lane == 0) {
-    int it = 0, acc = 0;
+    int it = 0, acc = 0, a_loads = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < p.num_tiles && ok; tile += gridDim.x, ++acc) {
+    const uint64_t a_desc0 = sdesc_sw128(c.sbase + OFF_A, 16, 1024);
+    const uint64_t b_desc0 = sdesc_sw128(c.sbase + OFF_B, B_PANEL, 1024);
+    for (int tile = tbeg; tile < tend && ok; ++tile, ++acc) {
+      const int h = tile % H;
+      if (tile == tbeg || h == 0) {
+        if (!c.wait(LF, a_loads & 1)) { ok = false; break; }
+        ++a_loads;
+      }
       const int a = acc & 1;
       if (acc >= 2 && !c.wait(AEMPTY + a, ((acc >> 1) - 1) & 1)) { ok = false; break; }
       tc_fence_after();
@@ -121,15 +153,19 @@ up_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         const int s = it % NS;
         if (!c.wait(FULL + s, (it / NS) & 1)) { ok = false; break; }
         tc_fence_after();
+        const uint64_t ad = a_desc0 + (uint64_t)(kb * A_PANEL >> 4);
+        const uint64_t bd = b_desc0 + (uint64_t)(s * B_BYTES >> 4);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(c.sbase + OFF_A + s * A_BYTES + kk * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(c.sbase + OFF_B + s * B_BYTES + kk * 16 * 128, B_PANEL, 1024);
-          mma_ss(tmem + a * BN, ad, bd, IDESC, (kb > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < BK / 16; ++kk)
+          mma_ss(tmem + a * BN, ad + (uint64_t)(kk * 32 >> 4), bd + (uint64_t)(kk * 16 * 128 >> 4), IDESC,
+                 (kb > 0 || kk > 0) ? 1u : 0u);
         tc_commit(c.bar(EMPTY + s));
       }
-      if (ok) tc_commit(c.bar(AFULL + a));
+      if (!ok) break;
+      tc_commit(c.bar(AFULL + a));
+      // The latent tile is free once the last head of its token block (in this CTA's
+      // range) has been multiplied.
+      if (tile + 1 == tend || h == H - 1) tc_commit(c.bar(LE));
     }
     tc_commit(c.bar(FIN));
     c.drain(FIN, 0);
@@ -137,38 +173,45 @@ up_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     const int quad = warp & 3, row = quad * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
     int acc = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++acc) {
+    uint4 rope[8];
+    for (int tile = tbeg; tile < tend; ++tile, ++acc) {
       const int a = acc & 1;
+      const int64_t t = (int64_t)(tile / H) * BM + row;
+      const int h = tile % H;
+      const bool live = t < p.num_tokens;
+      if ((tile == tbeg || h == 0) && live) {   // rope part of this token, the same for every head
+        const uint4* src = reinterpret_cast<const uint4*>(p.latent + t * 576 + 512);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rope[i] = __ldg(src + i);
+      }
       if (!__all_sync(0xffffffffu, c.wait(AFULL + a, (acc >> 1) & 1))) break;
       tc_fence_after();
-      const int64_t t = (int64_t)(tile / p.num_heads) * BM + row;
-      const int h = tile % p.num_heads;
-      const bool live = t < p.num_tokens;
-      const int64_t kr = (t * p.num_heads + h) * 192, vr = (t * p.num_heads + h) * 128;
+      const int64_t kr = (t * H + h) * 192, vr = (t * H + h) * 128;
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t r[64];
         tmem_ld64_sync(lane_addr + a * BN + ch * 64, r);
         if (live) {
-          uint4* dst = reinterpret_cast<uint4*>(ch < 2 ? p.k + kr + ch * 64 : p.v + vr + (ch - 2) * 64);
+          uint32_t w[32];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(r[8 * i + 0]), __uint_as_float(r[8 * i + 1]));
-            w.y = pack_bf16x2(__uint_as_float(r[8 * i + 2]), __uint_as_float(r[8 * i + 3]));
-            w.z = pack_bf16x2(__uint_as_float(r[8 * i + 4]), __uint_as_float(r[8 * i + 5]));
-            w.w = pack_bf16x2(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7]));
-            dst[i] = w;
+          for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+          char* dst = reinterpret_cast<char*>(ch < 2 ? p.k + kr + ch * 64 : p.v + vr + (ch - 2) * 64);
+          if (p.out_align32) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) st_global_v8(dst + q * 32, w + 8 * q);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              reinterpret_cast<uint4*>(dst)[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
           }
         }
       }
       tc_fence_before();
       mbar_arrive(c.bar(AEMPTY + a));
       if (live) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.latent + t * 576 + 512);
         uint4* dst = reinterpret_cast<uint4*>(p.k + kr + 128);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) dst[i] = __ldg(src + i);
+        for (int i = 0; i < 8; ++i) dst[i] = rope[i];
       }
     }
   }
@@ -204,6 +247,7 @@ cudaError_t launch_up_proj(const CUtensorMap& ta, const CUtensorMap& tb, const v
   p.status = status;
   p.num_tokens = num_tokens;
   p.num_heads = num_heads;
+  p.out_align32 = ((reinterpret_cast<uintptr_t>(k_out) | reinterpret_cast<uintptr_t>(v_out)) & 31u) == 0;
   const int64_t m_tiles = (num_tokens + BM - 1) / BM;
   p.num_tiles = (int)(m_tiles * num_heads);
   if (p.num_tiles == 0) return cudaSuccess;

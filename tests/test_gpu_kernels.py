@@ -66,8 +66,8 @@ def test_gather_bad_block_id_flags_and_zeroes():
 
 @pytest.mark.parametrize("entry_dim", [8, 72, 18432, 18440])
 def test_gather_row_widths(entry_dim):
-    # 16-byte rows up to 36 KB go through the bulk-copy kernel (several rows per CTA,
-    # partial last batch); wider rows take the register-vector kernel.
+    # 16-byte rows up to 36 KB go through the bulk-copy kernel (one or several rows per
+    # CTA, partial last batch); wider rows take the register-vector kernel.
     mla = _mla()
     rng = np.random.default_rng(entry_dim)
     num_blocks, block_size = 7, 4
