@@ -9,9 +9,10 @@
 // Design (one persistent CTA per SM, one work unit = 128 query rows of one head):
 //   warps 0, 10 TMA producers: warp 0 loads the Q tile once per unit and K tiles of 128
 //               keys, warp 10 V tiles, each through a two-stage ring.
-//   warp 1      MMA issuer (one thread): S = Q K^T into one of two TMEM S buffers
-//               (tcgen05.mma, both operands from shared memory), then O += P V with P
-//               read from TMEM (written there by the softmax warps over the S buffer).
+//   warps 1, 11 MMA issuers (one thread each): warp 1 issues S = Q K^T into one of two
+//               TMEM S buffers (tcgen05.mma, both operands from shared memory), warp 11
+//               O += P V with P read from TMEM (written there by the softmax warps over
+//               the S buffer).
 //   warps 2-9   softmax: two threads per query row (= one TMEM lane), each owning 64
 //               of the tile's 128 key columns and 64 of O's 128 columns.  Online
 //               softmax in base 2; O in TMEM is rescaled only when the running max
@@ -46,15 +47,16 @@ enum Bar {
   VE = 8,               // [stage] V tile released
   SF = 10,              // [S buffer] S = Q K^T done
   OD = 12,              // O += P V done
-  FIN = 13,             // all MMAs drained before TMEM is released
-  XM = 14, XL = 16,     // softmax half-row exchanges (max per tile, sum per unit)
-  NBAR = 17
+  SE = 13,              // [S buffer] P V done reading P: S may be overwritten
+  FINQ = 15, FINP = 16, // all MMAs of each issuer drained before TMEM is released
+  XM = 17, XL = 19,     // softmax half-row exchanges (max per tile, sum per unit)
+  NBAR = 20
 };
 constexpr int OFF_XCHG = OFF_BAR + NBAR * 8;      // row-max / row-sum exchange, 6 x 128 floats
 constexpr int OFF_MISC = OFF_XCHG + 6 * 128 * 4;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + slack for 1024-byte alignment
 
-constexpr int NTHREADS = 352;                       // Q/K producer, MMA, 8 softmax warps, V producer
+constexpr int NTHREADS = 384;   // Q/K producer, S issuer, 8 softmax warps, V producer, O issuer
 constexpr uint32_t TMEM_COLS = 512;
 __device__ __forceinline__ constexpr uint32_t TM_S(int b) { return b ? 128u : 0u; }
 constexpr uint32_t TM_O = 256;
@@ -151,29 +153,16 @@ __device__ void run_producer_v(const Ctx& c, const PrefillParams& p, const CUten
 }
 
 // ------------------------------------------------------------------ MMA issuer
-__device__ void run_mma(const Ctx& c, const PrefillParams& p, uint32_t tmem, int ubeg, int uend) {
-  int q_g = 0, kv_g = 0, s_g = 0;
+// Two MMA issuers.  A tcgen05.mma issue returns only once the tensor pipe takes the
+// instruction, so every wait of an issuing thread leaves the pipe idle unless another
+// thread has products queued: warp 1 issues S = Q K^T, warp 11 issues O += P V, and
+// each one's waits hide behind the other's products.  S of tile g + 2 reuses the S
+// buffer whose P the product of tile g reads, which the SE barrier orders.
+__device__ void run_mma_qk(const Ctx& c, const PrefillParams& p, uint32_t tmem, int ubeg, int uend) {
+  int q_g = 0, kv_g = 0;
   bool ok = true;
   const uint64_t q_desc = sdesc_sw128(c.sbase + OFF_Q, 16, 1024);
   const uint64_t k_desc0 = sdesc_sw128(c.sbase + OFF_K, 16, 1024);
-  const uint64_t v_desc0 = sdesc_sw128(c.sbase + OFF_V, PANEL, 1024);
-  auto issue_pv = [&](int t_local, int kv_base, int s_base) -> bool {
-    // Tiles are counted alike for S buffers and V stages (both advance once per tile),
-    // so one barrier per parity covers "P written" and "V landed".
-    const int sg = s_base + t_local, b = sg & 1;
-    const int g = kv_base + t_local, s = g % NSTAGE;
-    if (!c.wait(PV + b, (sg >> 1) & 1)) return false;
-    tc_fence_after();
-    const uint64_t vd = v_desc0 + (uint64_t)(s * V_PANELS * PANEL >> 4);
-#pragma unroll
-    for (int kk = 0; kk < BN / 16; ++kk) {
-      const uint64_t bd = vd + (uint64_t)(kk * 16 * 128 >> 4);
-      mma_ts(tmem + TM_O, tmem + TM_S(b) + kk * 8, bd, IDESC_PV, (t_local > 0 || kk > 0) ? 1u : 0u);
-    }
-    tc_commit(c.bar(VE + s));
-    tc_commit(c.bar(OD));
-    return true;
-  };
   for (int ui = ubeg; ui < uend && ok; ++ui) {
     const Unit u = load_unit(p.units, ui);
     const int lo = u.kv_tiles & 0xFFFF, hi = (u.kv_tiles >> 16) & 0xFFFF;
@@ -181,32 +170,54 @@ __device__ void run_mma(const Ctx& c, const PrefillParams& p, uint32_t tmem, int
     if (n <= 0) continue;
     if (!c.wait(QF, q_g & 1)) { ok = false; break; }
     ++q_g;
-    tc_fence_after();
     for (int j = 0; j < n && ok; ++j) {
-      const int g = kv_g + j, s = g % NSTAGE;
+      const int g = kv_g + j, s = g % NSTAGE, b = g & 1;
       if (!c.wait(KF + s, (g / NSTAGE) & 1)) { ok = false; break; }
+      if (g >= 2 && !c.wait(SE + b, ((g - 2) >> 1) & 1)) { ok = false; break; }
       tc_fence_after();
-      const int b = (s_g + j) & 1;
       const uint64_t kd = k_desc0 + (uint64_t)(s * K_PANELS * PANEL >> 4);
 #pragma unroll
       for (int kk = 0; kk < 192 / 16; ++kk) {
         const uint64_t off = (uint64_t)(((kk >> 2) * PANEL + (kk & 3) * 32) >> 4);
-        const uint64_t ad = q_desc + off;
-        const uint64_t bd = kd + off;
-        mma_ss(tmem + TM_S(b), ad, bd, IDESC_QK, kk > 0 ? 1u : 0u);
+        mma_ss(tmem + TM_S(b), q_desc + off, kd + off, IDESC_QK, kk > 0 ? 1u : 0u);
       }
       tc_commit(c.bar(SF + b));
       tc_commit(c.bar(KE + s));
       if (j == n - 1) tc_commit(c.bar(QE));
-      if (j > 0 && !issue_pv(j - 1, kv_g, s_g)) { ok = false; break; }
     }
-    if (ok && !issue_pv(n - 1, kv_g, s_g)) ok = false;
     kv_g += n;
-    s_g += n;
   }
   // Every MMA issued by this thread must finish before TMEM is released.
-  tc_commit(c.bar(FIN));
-  c.drain(FIN, 0);
+  tc_commit(c.bar(FINQ));
+  c.drain(FINQ, 0);
+}
+
+__device__ void run_mma_pv(const Ctx& c, const PrefillParams& p, uint32_t tmem, int ubeg, int uend) {
+  int g = 0;
+  bool ok = true;
+  const uint64_t v_desc0 = sdesc_sw128(c.sbase + OFF_V, PANEL, 1024);
+  for (int ui = ubeg; ui < uend && ok; ++ui) {
+    const Unit u = load_unit(p.units, ui);
+    const int lo = u.kv_tiles & 0xFFFF, hi = (u.kv_tiles >> 16) & 0xFFFF;
+    const int n = hi - lo;
+    for (int j = 0; j < n; ++j, ++g) {
+      // Tiles are counted alike for S buffers and V stages (both advance once per
+      // tile), so one barrier per parity covers "P written" and "V landed".
+      const int b = g & 1, s = g % NSTAGE;
+      if (!c.wait(PV + b, (g >> 1) & 1)) { ok = false; break; }
+      tc_fence_after();
+      const uint64_t vd = v_desc0 + (uint64_t)(s * V_PANELS * PANEL >> 4);
+#pragma unroll
+      for (int kk = 0; kk < BN / 16; ++kk)
+        mma_ts(tmem + TM_O, tmem + TM_S(b) + kk * 8, vd + (uint64_t)(kk * 16 * 128 >> 4), IDESC_PV,
+               (j > 0 || kk > 0) ? 1u : 0u);
+      tc_commit(c.bar(VE + s));
+      tc_commit(c.bar(SE + b));
+      tc_commit(c.bar(OD));
+    }
+  }
+  tc_commit(c.bar(FINP));
+  c.drain(FINP, 0);
 }
 
 // ------------------------------------------------------------------ softmax
@@ -404,9 +415,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   if (warp == 0) {
     if (lane == 0) run_producer_qk(c, p, &tm_q, &tm_k, ubeg, uend);
   } else if (warp == 1) {
-    if (lane == 0) run_mma(c, p, tmem, ubeg, uend);
+    if (lane == 0) run_mma_qk(c, p, tmem, ubeg, uend);
   } else if (warp == 10) {
     if (lane == 0) run_producer_v(c, p, &tm_v, ubeg, uend);
+  } else if (warp == 11) {
+    if (lane == 0) run_mma_pv(c, p, tmem, ubeg, uend);
   } else {
     run_softmax(c, p, tmem, reinterpret_cast<float*>(smem + OFF_XCHG), ubeg, uend);
   }

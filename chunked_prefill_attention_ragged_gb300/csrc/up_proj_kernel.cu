@@ -15,7 +15,8 @@
 // of 384 KB, below what L2 delivers to one SM.
 //   warp 0     TMA producer: the latent tile when the token block changes (8 K-major
 //              panels of 128 x 64), and W's slice as [64 x 256] blocks (4 N-major
-//              panels of 64 x 64) through a 3-stage ring.
+//              panels of 64 x 64) through a 3-stage ring, marked evict-last in L2 (the
+//              K/V output is stored evict-first), so W is read from HBM about once.
 //   warp 1     MMA issuer: tcgen05.mma M=128 N=256 K=16 into one of two TMEM
 //              accumulators (512 columns), so the epilogue of tile i overlaps the
 //              MMAs of tile i+1.
@@ -113,6 +114,9 @@ up_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
   if (warp == 0 && lane == 0) {
     int it = 0, a_loads = 0;
     bool ok = true;
+    // W (32 MB for 128 heads) is read by every token block: keep it in L2 while the
+    // much larger K/V output streams through.
+    const uint64_t w_policy = l2_policy_evict_last();
     for (int tile = tbeg; tile < tend && ok; ++tile) {
       const int m = tile / H, h = tile % H;
       if (tile == tbeg || h == 0) {   // new token block: reload the latent tile
@@ -128,8 +132,8 @@ up_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
         if (use > 0 && !c.wait(EMPTY + s, (use - 1) & 1)) { ok = false; break; }
         mbar_arrive_expect_tx(c.bar(FULL + s), B_BYTES);
         for (int i = 0; i < 4; ++i)
-          tma_load_2d(c.sbase + OFF_B + s * B_BYTES + i * B_PANEL, &tm_b, c.bar(FULL + s),
-                      h * BN + i * 64, kb * BK);
+          tma_load_2d_hint(c.sbase + OFF_B + s * B_BYTES + i * B_PANEL, &tm_b, c.bar(FULL + s),
+                           h * BN + i * 64, kb * BK, w_policy);
       }
     }
     if (a_loads > 0) c.drain(LF, (a_loads - 1) & 1);
@@ -174,6 +178,7 @@ up_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
     int acc = 0;
     uint4 rope[8];
+    const uint64_t out_policy = l2_policy_evict_first();   // K/V are written once here
     for (int tile = tbeg; tile < tend; ++tile, ++acc) {
       const int a = acc & 1;
       const int64_t t = (int64_t)(tile / H) * BM + row;
@@ -198,7 +203,7 @@ up_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
           char* dst = reinterpret_cast<char*>(ch < 2 ? p.k + kr + ch * 64 : p.v + vr + (ch - 2) * 64);
           if (p.out_align32) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) st_global_v8(dst + q * 32, w + 8 * q);
+            for (int q = 0; q < 4; ++q) st_global_v8_hint(dst + q * 32, w + 8 * q, out_policy);
           } else {
 #pragma unroll
             for (int q = 0; q < 8; ++q)
