@@ -9,10 +9,14 @@ chunk's LSE so the partial outputs can be merged.  sglang issue #3849: the
 prefix lives in the paged cache as 512 latent + 64 rope per token and is
 decompressed before attention.
 
-Per run: new-token attention -> for every chunk: gather -> up-projection ->
-non-causal attention -> in-place LSE merge into the running (O, LSE).  Every
-step is a kernel of libmla_prefill.so; this class only owns buffers and
-orders the calls on one stream.
+Per run: new-token attention -> one gather of every chunk's latent rows ->
+for every chunk: up-projection -> non-causal attention -> in-place LSE merge
+into the running (O, LSE).  Chunking bounds the decompressed K/V (per chunk
+tokens x heads x 640 bytes); the compressed rows are small (1152 bytes per
+token), so all chunks are gathered by one launch, which keeps that copy large
+enough to run near HBM bandwidth.  Every step is a kernel of
+libmla_prefill.so; this class only owns buffers and orders the calls on one
+stream.
 """
 from __future__ import annotations
 
@@ -46,25 +50,64 @@ class ChunkedPrefill:
         self.chunk_tokens = [int(cu[c, -1]) for c in range(cu.shape[0])]
         self.cu_dev = torch.from_numpy(cu.copy()).to(device)
         self.starts_dev = torch.from_numpy(st.copy()).to(device)
+        # All chunks in one gather: (chunk, request) pairs become the rows' "requests",
+        # chunk c's rows are latent[row0[c] : row0[c] + chunk_tokens[c]], and the block
+        # table is repeated once per chunk.
+        n_chunks, batch = cu.shape[0], cu.shape[1] - 1
+        self.num_chunks, self.batch = n_chunks, batch
+        self.row0 = [0]
+        for t in self.chunk_tokens:
+            self.row0.append(self.row0[-1] + t)
+        lens_all = np.diff(cu, axis=1).reshape(-1)
+        cu_all = np.zeros(n_chunks * batch + 1, dtype=np.int32)
+        np.cumsum(lens_all, out=cu_all[1:])
+        self.cu_all_dev = torch.from_numpy(cu_all).to(device)
+        self.starts_all_dev = torch.from_numpy(st.reshape(-1).astype(np.int32).copy()).to(device)
+        self.total_prefix = int(cu_all[-1])
+        self.table_all = None
+        self._table_key = None
         t_max = max(self.chunk_tokens, default=0)
         h = num_heads
         bf = torch.bfloat16
-        self.latent = torch.empty((max(t_max, 1), 576), dtype=bf, device=device)
+        self.latent = torch.empty((max(self.total_prefix, 1), 576), dtype=bf, device=device)
         self.k_c = torch.empty((max(t_max, 1), h, 192), dtype=bf, device=device)
         self.v_c = torch.empty((max(t_max, 1), h, 128), dtype=bf, device=device)
         self.o_c = torch.empty((max(self.total_q, 1), h, 128), dtype=bf, device=device)
         self.lse_c = torch.empty((max(self.total_q, 1), h), dtype=torch.float32, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
 
+    def chunk_table(self, block_table):
+        """The block table repeated once per chunk (rows of the one gather launch).
+
+        Rebuilt only when the caller's table changed (another tensor, or written in
+        place since the last call), so layers that share a batch's table pay once."""
+        import torch
+        key = (block_table.data_ptr(), block_table._version, tuple(block_table.shape), block_table.device)
+        if self.table_all is not None and key == self._table_key:
+            return self.table_all
+        shape = (self.num_chunks * self.batch, block_table.shape[1])
+        self.table_all = torch.empty(shape, dtype=torch.int32, device=block_table.device)
+        self.table_all.view(self.num_chunks, self.batch, -1).copy_(block_table.unsqueeze(0).expand(
+            self.num_chunks, -1, -1))
+        self._table_key = key
+        return self.table_all
+
+    def gather_all(self, cache, block_table, stream=None):
+        """Every chunk's latent rows, one launch: self.latent[row0[c]:row0[c+1]] is chunk c."""
+        if self.total_prefix:
+            mla_gather_latent(cache, self.chunk_table(block_table), self.cu_all_dev, self.starts_all_dev,
+                              self.total_prefix, self.latent[:self.total_prefix], self.status, stream)
+        return self.latent
+
     def run(self, q, k, v, cache, block_table, w_kvb, o=None, lse=None, stream=None):
         """q/k/v: new tokens; cache [NB, BS, 576]; block_table [B, M] int32 (device)."""
         o, lse = self.main.run(q, k, v, o, lse, True, stream)
+        self.gather_all(cache, block_table, stream)
         for c, plan in enumerate(self.chunks):
             t = self.chunk_tokens[c]
             if t == 0:
                 continue
-            lat = self.latent[:t]
-            mla_gather_latent(cache, block_table, self.cu_dev[c], self.starts_dev[c], t, lat, self.status, stream)
+            lat = self.latent[self.row0[c]:self.row0[c] + t]
             kc, vc = self.k_c[:t], self.v_c[:t]
             mla_up_proj(lat, w_kvb, self.num_heads, kc, vc, self.status, stream)
             oc, lc = self.o_c[:self.total_q], self.lse_c[:self.total_q]

@@ -121,7 +121,7 @@ def random_ragged(seed: int, q_lens, kv_lens=None, num_heads: int = 4, *,
 
 WORKLOAD_NAMES = (
     "tiny_ragged_causal",            # 0
-    "r1_ragged_8x_u512_4096_h128",   # 1
+    "deepseek_ragged_8x_u512_4096_h128",   # 1
     "chunked_prefix_4x2048_p8192",   # 2
     "long_single_32768_h128",        # 3
     "many_short_256_geo200_h16",     # 4

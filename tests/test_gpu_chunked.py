@@ -46,3 +46,23 @@ def test_workload2_sampled():
     idx = torch.from_numpy(np.concatenate([b.qo_indptr[r] + rows[r] for r in range(b.batch)])).cuda()
     check_attention(f64_of_bf16(o[idx][:, heads]), lse[idx][:, heads].double().cpu().numpy(), o_ref, lse_ref,
                     "workload2")
+
+
+def test_all_chunk_gather_matches_oracle_per_chunk():
+    # The pipeline gathers every chunk's latent rows with one launch; chunk c's rows must
+    # equal the oracle's gather of that chunk alone, bit for bit.
+    from chunked_prefill_attention_ragged_gb300.pipeline import ChunkedPrefill
+    from oracle import gather_latent
+    cb = wl.random_chunked_prefix(41, [30, 5, 17], [300, 1, 129], 2, num_blocks=40, block_size=16,
+                                  chunk_tokens=100)
+    b = cb.new
+    pipe = ChunkedPrefill(b.qo_indptr, cb.layout.cu_seq_lens, cb.layout.chunk_starts, b.num_heads,
+                          sm_scale=b.sm_scale)
+    table = torch.from_numpy(cb.block_table).cuda()
+    lat = pipe.gather_all(to_dev_bf16(cb.cache), table)
+    torch.cuda.synchronize()
+    pipe.check_status()
+    got = lat.view(torch.int16).cpu().numpy().view(np.uint16)
+    for c in range(cb.layout.num_chunks):
+        ref = gather_latent(cb.cache, cb.block_table, cb.layout.cu_seq_lens[c], cb.layout.chunk_starts[c])
+        np.testing.assert_array_equal(got[pipe.row0[c]:pipe.row0[c + 1]], ref)
