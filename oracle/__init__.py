@@ -14,6 +14,8 @@ computes, written from the pages' definitions:
     block_size + pos % block_size, from the decode branch of
     ``_build_c128a_topk_metadata_kernel`` in vLLM's
     ``vllm/models/deepseek_v4/sparse_mla.py``);
+  * the paged cache write of new tokens' compressed rows by slot mapping
+    (negative slot = padding token, sglang issue #3849 / vLLM sparse_mla.py);
   * the latent up-projection into per-head K = [K_nope || k_rope] and V
     (sglang issue #3849: 512 latent + 64 rope cached, attention runs as MHA
     with 192-dim Q/K and 128-dim V);
@@ -28,19 +30,21 @@ or from hand-written fixtures.
 
 Every function here is pinned by ``-m "not gpu"`` tests against brute force,
 closed forms and invariants.  Parity pins: attention (brute force, closed
-forms, invariants), gather (hand fixture + brute force), up-projection
+forms, invariants), gather (hand fixture + brute force), cache write (hand
+fixture, round trip through the gather, padding slots), up-projection
 (hand fixture + triple loop), merge (closed forms + split/merge identity),
 chunked pipeline (split/merge identity).  No function is "parity unpinned".
 """
 from .bf16 import bf16_bits_to_f64, round_f64_to_bf16
 from .attention import allowed_mask, attend_request, ragged_attention
 from .gather import gather_latent, slot_of
+from .cache_write import cache_write
 from .up_proj import up_project
 from .merge import merge_state
 from .chunked import chunked_prefill_attention
 
 __all__ = [
     "bf16_bits_to_f64", "round_f64_to_bf16", "allowed_mask", "attend_request",
-    "ragged_attention", "gather_latent", "slot_of", "up_project", "merge_state",
+    "ragged_attention", "gather_latent", "slot_of", "cache_write", "up_project", "merge_state",
     "chunked_prefill_attention",
 ]
