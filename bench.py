@@ -449,6 +449,26 @@ def bench_chunked(args, dev, peaks):
         torch.cuda.synchronize()
         iso.append(e0.elapsed_time(e1))
     pipe.check_status()
+    # Cache write of the new tokens' compressed rows (slot mapping into blocks the prefix
+    # does not use), timed alone like the gather.
+    n_new = int(b.q.shape[0])
+    free_blocks = np.setdiff1d(np.arange(cb.cache.shape[0]), cb.block_table.ravel())
+    bs = cb.cache.shape[1]
+    slots_h = np.concatenate([free_blocks[:(n_new + bs - 1) // bs, None] * bs + np.arange(bs)[None, :]]).ravel()
+    slots = torch.from_numpy(slots_h[:n_new].astype(np.int64)).to(dev)
+    new_latent = torch.randn(n_new, 576, device=dev).to(torch.bfloat16)
+    cw = []
+    for _ in range(10):
+        flush.zero_()
+        flush_read.sum()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        mla.mla_cache_write(cache, new_latent, slots, pipe.status)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        cw.append(e0.elapsed_time(e1))
+    pipe.check_status()
+    cw_bytes = 2 * n_new * 576 * 2
     del flush_read
     med = {n: statistics.median(x) for n, x in acc.items()}
     T = int(pipe.chunk_tokens[0])
@@ -479,6 +499,10 @@ def bench_chunked(args, dev, peaks):
                             "gbs": round(gather_bytes / statistics.median(iso) / 1e6, 1),
                             "frac_hbm": round(gather_bytes / statistics.median(iso) / 1e6 / hbm, 3),
                             "l2": "256 MB written, then another 256 MB read, before each launch"},
+        "cache_write": {"ms": round(statistics.median(cw), 4), "tokens": n_new,
+                        "gbs": round(cw_bytes / statistics.median(cw) / 1e6, 1),
+                        "frac_hbm": round(cw_bytes / statistics.median(cw) / 1e6 / hbm, 3),
+                        "l2": "256 MB written, then another 256 MB read, before each launch"},
         "merge": {"ms": round(med["merge"], 4), "gbs": round(merge_bytes / med["merge"] / 1e6, 1),
                   "frac_hbm": round(merge_bytes / med["merge"] / 1e6 / hbm, 3)},
         "hbm_peak_gbs": hbm, "hbm_peak_source": peaks["source"],

@@ -36,6 +36,7 @@ _SIGNATURES = {
                                      _i64p]),
     "mla_gather_latent": (_c_int, [_c_vp, _c_i64, _c_int, _c_int, _c_vp, _c_int, _c_vp, _c_vp, _c_int, _c_i64,
                                    _c_vp, _c_vp, _c_vp]),
+    "mla_cache_write": (_c_int, [_c_vp, _c_i64, _c_int, _c_int, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp]),
     "mla_up_proj": (_c_int, [_c_vp, _c_vp, _c_i64, _c_int, _c_vp, _c_vp, _c_vp, _c_vp]),
     "mla_merge_state": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_int, _c_int, _c_vp]),
     "mla_prefill_run_noalloc": (_c_int, [_i32p, _i32p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_f, _c_int, _c_f,
@@ -232,6 +233,21 @@ def mla_gather_latent(cache, block_table, cu_seq_lens, chunk_starts, total_token
                                        batch, int(total_tokens), _dev(out, torch.bfloat16, "out"),
                                        _dev(status, i32, "status"), _stream(stream)), "mla_gather_latent")
     return out
+
+
+def mla_cache_write(cache, latent, slot_mapping, status=None, stream=None):
+    """Store latent [T, E] rows into the paged cache [NB, BS, E] at slot_mapping [T] (int64,
+    device; negative = padding token).  Returns the cache (written in place)."""
+    import torch
+    nb, bs, e = cache.shape
+    t = latent.shape[0]
+    if latent.shape[1] != e or slot_mapping.shape[0] != t:
+        raise ValueError("latent must be [T, entry_dim] and slot_mapping [T]")
+    _check(library().mla_cache_write(_dev(cache, torch.bfloat16, "cache"), nb, bs, e,
+                                     _dev(latent, torch.bfloat16, "latent"),
+                                     _dev(slot_mapping, torch.int64, "slot_mapping"), int(t),
+                                     _dev(status, torch.int32, "status"), _stream(stream)), "mla_cache_write")
+    return cache
 
 
 def mla_up_proj(latent, w_kvb, num_heads: int, k_out=None, v_out=None, status=None, stream=None):

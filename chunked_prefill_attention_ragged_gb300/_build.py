@@ -27,6 +27,7 @@ SOURCES = [
     "tma.cpp",
     "attn_kernel.cu",
     "gather_kernel.cu",
+    "cache_write_kernel.cu",
     "merge_kernel.cu",
     "up_proj_kernel.cu",
     "noalloc.cu",

@@ -43,6 +43,10 @@ cudaError_t launch_gather(const void* cache, int64_t num_blocks, int block_size,
                           const int32_t* cu_seq_lens, const int32_t* chunk_starts, int batch,
                           int64_t total_tokens, void* out, int32_t* status, cudaStream_t stream);
 
+cudaError_t launch_cache_write(void* cache, int64_t num_slots, int entry_dim, const void* latent,
+                               const int64_t* slot_mapping, int64_t num_tokens, int32_t* status,
+                               cudaStream_t stream);
+
 int up_proj_smem_bytes();
 cudaError_t launch_up_proj(const CUtensorMap& ta, const CUtensorMap& tb, const void* latent,
                            int64_t num_tokens, int num_heads, void* k_out, void* v_out,

@@ -229,6 +229,21 @@ int mla_gather_latent(const void* cache, int64_t num_blocks, int block_size, int
              : MLA_ERR_CUDA;
 }
 
+int mla_cache_write(void* cache, int64_t num_blocks, int block_size, int entry_dim, const void* latent,
+                    const int64_t* slot_mapping, int64_t num_tokens, int32_t* status, void* stream) {
+  if (num_tokens < 0 || num_blocks < 0 || block_size < 1 || entry_dim < 8 || entry_dim % 8 != 0)
+    return MLA_ERR_INVALID_ARG;
+  if ((int64_t)entry_dim * 2 > 200 * 1024) return MLA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return MLA_OK;
+  if (!cache || !latent || !slot_mapping || !aligned16(cache) || !aligned16(latent) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0 || (reinterpret_cast<uintptr_t>(status) & 3u) != 0)
+    return MLA_ERR_INVALID_ARG;
+  return launch_cache_write(cache, num_blocks * (int64_t)block_size, entry_dim, latent, slot_mapping, num_tokens,
+                            status, as_stream(stream)) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
 int mla_up_proj(const void* latent, const void* w_kvb, int64_t num_tokens, int num_heads, void* k_out,
                 void* v_out, int32_t* status, void* stream) {
   if (num_tokens < 0 || num_heads < 1) return MLA_ERR_INVALID_ARG;

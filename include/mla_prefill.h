@@ -166,6 +166,29 @@ MLA_API int mla_gather_latent(const void* cache, int64_t num_blocks, int block_s
                       int64_t total_tokens, void* out, int32_t* status, void* stream);
 
 /* ======================================================================
+ * Paged latent cache write.  [sglang] ragged prefill saves the new tokens'
+ * compressed rows (512 latent + 64 rope) in the cache before attention;
+ * [vLLM-V4] a token's flat slot is block * block_size + offset, and a
+ * negative slot marks a padding token.
+ * ====================================================================== */
+/*
+ *   cache        : bf16 [num_blocks, block_size, entry_dim] (entry_dim % 8 == 0, at most
+ *                  102400; 576 for MLA), written in place
+ *   latent       : bf16 [num_tokens, entry_dim], the new tokens' rows
+ *   slot_mapping : DEVICE int64 [num_tokens]; row t goes to flat slot slot_mapping[t]
+ *                  (block = slot / block_size, offset = slot % block_size); a negative
+ *                  slot writes nothing; a slot >= num_blocks * block_size writes nothing
+ *                  and ORs MLA_DEVSTAT_BAD_INDEX into status
+ *   status       : DEVICE int32 word or NULL
+ * Bit-exact copy; allocates nothing.  If two tokens name the same slot, the row left
+ * there is one of theirs (unspecified which).  Pointers: cache and latent 16-byte
+ * aligned, slot_mapping 8-byte aligned.
+ */
+MLA_API int mla_cache_write(void* cache, int64_t num_blocks, int block_size, int entry_dim,
+                            const void* latent, const int64_t* slot_mapping, int64_t num_tokens,
+                            int32_t* status, void* stream);
+
+/* ======================================================================
  * Latent up-projection.  [sglang] 512 latent + 64 rope -> MHA K (192) / V (128).
  * ====================================================================== */
 /*

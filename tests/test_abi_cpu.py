@@ -72,6 +72,13 @@ def test_entry_points_reject_null_and_misaligned():
     assert lib.mla_up_proj(None, None, 0, 4, None, None, None, None) == 0
     assert lib.mla_up_proj(None, None, 8, 4, None, None, None, None) == -1
     assert lib.mla_up_proj(16, 16, 8, 4, 16, 24, None, None) == -1   # misaligned v_out
+    # cache write: shapes first, then pointers; nothing reaches the device
+    assert lib.mla_cache_write(None, 4, 64, 576, None, None, 0, None, None) == 0
+    assert lib.mla_cache_write(None, 4, 64, 572, None, None, 8, None, None) == -1
+    assert lib.mla_cache_write(None, 4, 0, 576, None, None, 8, None, None) == -1
+    assert lib.mla_cache_write(None, 4, 64, 110000, None, None, 8, None, None) == -3
+    assert lib.mla_cache_write(None, 4, 64, 576, None, None, 8, None, None) == -1
+    assert lib.mla_cache_write(16, 4, 64, 576, 32, 12, 8, None, None) == -1   # misaligned slot_mapping
 
 
 def _coverage(units, qo, kv, heads, causal, window):

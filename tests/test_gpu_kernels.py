@@ -3,7 +3,7 @@ import numpy as np
 import pytest
 
 from chunked_prefill_attention_ragged_gb300 import workloads as wl
-from oracle import bf16_bits_to_f64, gather_latent, merge_state, round_f64_to_bf16, up_project
+from oracle import bf16_bits_to_f64, cache_write, gather_latent, merge_state, round_f64_to_bf16, up_project
 from gpu_util import bits_of, f64_of_bf16, to_dev, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
@@ -78,6 +78,69 @@ def test_gather_row_widths(entry_dim):
     out = mla.mla_gather_latent(to_dev_bf16(cache), to_dev(table), to_dev(cu), to_dev(st), int(cu[-1]))
     torch.cuda.synchronize()
     np.testing.assert_array_equal(bits_of(out), gather_latent(cache, table, cu, st))
+
+
+# ------------------------------------------------------------------ cache write
+def _slots(rng, n_tokens, num_slots, pad=0):
+    s = rng.permutation(num_slots)[:n_tokens].astype(np.int64)
+    if pad:
+        s[rng.choice(n_tokens, pad, replace=False)] = -1
+    return s
+
+
+@pytest.mark.parametrize("entry_dim,tokens,pad", [(576, 301, 17), (576, 1, 0), (8, 64, 5), (72, 33, 33),
+                                                  (18440, 7, 2), (32768, 5, 1)])
+def test_cache_write_bit_exact(entry_dim, tokens, pad):
+    # One or several rows per CTA (ragged last batch), padding slots, rows wider than the
+    # 48 KB default shared-memory limit.
+    mla = _mla()
+    rng = np.random.default_rng(entry_dim + tokens)
+    nb, bs = 40, 8
+    cache = rng.integers(0, 1 << 16, size=(nb, bs, entry_dim), dtype=np.uint16)
+    lat = rng.integers(0, 1 << 16, size=(tokens, entry_dim), dtype=np.uint16)
+    slots = _slots(rng, tokens, nb * bs, pad)
+    d_cache = to_dev_bf16(cache)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.mla_cache_write(d_cache, to_dev_bf16(lat), to_dev(slots), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    np.testing.assert_array_equal(bits_of(d_cache), cache_write(cache, lat, slots))
+
+
+def test_cache_write_bad_slot_is_flagged_and_skipped():
+    mla = _mla()
+    rng = np.random.default_rng(9)
+    cache = rng.integers(0, 1 << 16, size=(4, 16, 576), dtype=np.uint16)
+    lat = rng.integers(0, 1 << 16, size=(6, 576), dtype=np.uint16)
+    slots = np.array([3, 64, 10, 1000, -5, 63], dtype=np.int64)   # 64 and 1000 are past the cache
+    d_cache = to_dev_bf16(cache)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.mla_cache_write(d_cache, to_dev_bf16(lat), to_dev(slots), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 2
+    keep = slots.copy()
+    keep[(keep >= 64)] = -1
+    np.testing.assert_array_equal(bits_of(d_cache), cache_write(cache, lat, keep))
+
+
+def test_cache_write_then_gather_round_trip():
+    # New positions written through the slot rule come back out of the gather unchanged.
+    mla = _mla()
+    rng = np.random.default_rng(5)
+    nb, bs = 16, 16
+    cache = rng.integers(0, 1 << 16, size=(nb, bs, 576), dtype=np.uint16)
+    table = rng.permutation(nb)[:12].reshape(2, 6).astype(np.int32)   # 96 positions per request
+    starts, lens = [70, 33], [25, 40]
+    slots = np.array([int(table[r, p // bs]) * bs + p % bs for r in range(2)
+                      for p in range(starts[r], starts[r] + lens[r])], dtype=np.int64)
+    lat = rng.integers(0, 1 << 16, size=(len(slots), 576), dtype=np.uint16)
+    d_cache = to_dev_bf16(cache)
+    mla.mla_cache_write(d_cache, to_dev_bf16(lat), to_dev(slots))
+    cu = wl.indptr_from_lengths(lens)
+    back = mla.mla_gather_latent(d_cache, to_dev(table), to_dev(cu), to_dev(np.array(starts, dtype=np.int32)),
+                                 int(cu[-1]))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(bits_of(back), lat)
 
 
 # ------------------------------------------------------------------ up-projection
