@@ -175,6 +175,23 @@ def dist_env():
     return world, rank, local
 
 
+def reduce_max(x: float, world: int, device) -> float:
+    """The maximum of x over all ranks (x itself when there is one rank).  Each rank runs
+    its own batch (weak scaling), so the job's time is the slowest rank's."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tflops(flops_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank's FLOPs over the slowest rank's step time."""
+    return flops_per_rank * world / (ms_per_step * 1e-3) / 1e12
+
+
 # ----------------------------------------------------------------------------- CPU oracle timing
 def _oracle_job(args):
     """One (request, head) of the oracle; run in a spawned single-threaded worker."""
@@ -273,15 +290,10 @@ def bench_ours(args, world, rank, local):
         torch.cuda.synchronize()
         barrier()
     plan.status()
-    total_ms = t_start.elapsed_time(t_end)
+    total_ms = reduce_max(t_start.elapsed_time(t_end), world, dev)
     launch_ms = [a.elapsed_time(c) for a, c in ev]
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
-    value = flops * world / (ms_per_step * 1e-3) / 1e12
+    value = aggregate_tflops(flops, world, ms_per_step)
 
     # ---- end to end through the public API with host buffers
     pin = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).pin_memory()  # noqa: E731
@@ -310,7 +322,7 @@ def bench_ours(args, world, rank, local):
         keep.append(e2e_step())
     torch.cuda.synchronize()
     barrier()
-    e2e_s = (time.perf_counter() - t0) / e_steps
+    e2e_s = reduce_max((time.perf_counter() - t0) / e_steps, world, dev)
     del keep
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
     d2h = ho.numel() * 2 + hl.numel() * 4
@@ -359,7 +371,8 @@ def bench_ours(args, world, rank, local):
             "traffic": committed_traffic(),
             "avg_launch_ms": round(avg_launch_ms, 4),
         },
-        "e2e": {"value": round(flops / e2e_s / 1e12, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": round(aggregate_tflops(flops, world, e2e_s * 1e3), 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 3),
                 "includes": "pinned H2D of Q/K/V, plan, run, D2H of O/LSE"},
         "cpu_baseline": cpu,
