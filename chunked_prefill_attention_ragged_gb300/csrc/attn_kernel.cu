@@ -9,15 +9,16 @@
 // Design (one persistent CTA per SM, one work unit = 128 query rows of one head):
 //   warps 0, 10 TMA producers: warp 0 loads the Q tile once per unit and K tiles of 128
 //               keys, warp 10 V tiles, each through a two-stage ring.
-//   warps 1, 11 MMA issuers (one thread each): warp 1 issues S = Q K^T into one of two
-//               TMEM S buffers (tcgen05.mma, both operands from shared memory), warp 11
-//               O += P V with P read from TMEM (written there by the softmax warps over
-//               the S buffer).
+//   warps 1, 11 MMA issuers (one thread each): warp 1 issues S = Q K^T into one of three
+//               TMEM S buffers (tcgen05.mma, both operands from shared memory), so S
+//               runs up to two tiles ahead of the softmax; warp 11 issues O += P V with
+//               P read from TMEM (written there by the softmax warps over the S buffer).
 //   warps 2-9   softmax: two threads per query row (= one TMEM lane), each owning 64
 //               of the tile's 128 key columns and 64 of O's 128 columns.  Online
 //               softmax in base 2; O in TMEM is rescaled only when the running max
 //               grows by more than 2^8, so most tiles need no correction pass.
 //               Epilogue normalises O, writes it (bf16) and the natural-log LSE (fp32).
+// TMEM: S buffers 0-2 (128 columns each; P overwrites the front of its S as bf16), O.
 // Every pipeline wait is bounded: on time-out the CTA records MLA_DEVSTAT_TIMEOUT,
 // drains its own copies and MMAs, frees TMEM and returns.
 #include <cuda_bf16.h>
@@ -40,17 +41,19 @@ constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + Q_PANELS * PANEL;
 constexpr int OFF_V = OFF_K + NSTAGE * K_PANELS * PANEL;
 constexpr int OFF_BAR = OFF_V + NSTAGE * V_PANELS * PANEL;
+constexpr int NSB = 3;   // S buffers in TMEM
 enum Bar {
   QF = 0, QE = 1,       // Q landed / released
   KF = 2, KE = 4,       // [stage] K tile landed / released
-  PV = 6,               // [tile parity] V tile landed AND P written by all 8 softmax warps
+  VF = 6,               // [stage] V tile landed
   VE = 8,               // [stage] V tile released
   SF = 10,              // [S buffer] S = Q K^T done
-  OD = 12,              // O += P V done
-  SE = 13,              // [S buffer] P V done reading P: S may be overwritten
-  FINQ = 15, FINP = 16, // all MMAs of each issuer drained before TMEM is released
-  XM = 17, XL = 19,     // softmax half-row exchanges (max per tile, sum per unit)
-  NBAR = 20
+  OD = 13,              // O += P V done
+  SE = 14,              // [S buffer] P V done reading P: S may be overwritten
+  FINQ = 17, FINP = 18, // all MMAs of each issuer drained before TMEM is released
+  XM = 19, XL = 21,     // softmax half-row exchanges (max per tile, sum per unit)
+  PR = 22,              // [S buffer] P written by all 8 softmax warps
+  NBAR = 25
 };
 constexpr int OFF_XCHG = OFF_BAR + NBAR * 8;      // row-max / row-sum exchange, 6 x 128 floats
 constexpr int OFF_MISC = OFF_XCHG + 6 * 128 * 4;
@@ -58,8 +61,8 @@ constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + slack for 1024-byte alig
 
 constexpr int NTHREADS = 384;   // Q/K producer, S issuer, 8 softmax warps, V producer, O issuer
 constexpr uint32_t TMEM_COLS = 512;
-__device__ __forceinline__ constexpr uint32_t TM_S(int b) { return b ? 128u : 0u; }
-constexpr uint32_t TM_O = 256;
+__device__ __forceinline__ constexpr uint32_t TM_S(int b) { return (uint32_t)b * 128u; }
+constexpr uint32_t TM_O = 384;
 
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, 128, false, true);
@@ -94,9 +97,7 @@ __device__ __forceinline__ Unit load_unit(const Unit* units, int i) {
 // ------------------------------------------------------------------ producers
 // Two producer threads, so that a K load never queues behind a V load waiting for its
 // stage: warp 0 loads Q (once per unit) and K tiles, warp 10 loads V tiles.  A K stage
-// frees when its S = Q K^T is done, a V stage when its P V is done.  A V load lands on
-// the tile's PV barrier, which also counts the softmax warps' P arrivals, so the MMA
-// issuer waits once for both inputs of P V.
+// frees when its S = Q K^T is done, a V stage when its P V is done.
 __device__ void run_producer_qk(const Ctx& c, const PrefillParams& p, const CUtensorMap* tq,
                                 const CUtensorMap* tk, int ubeg, int uend) {
   int q_g = 0, k_g = 0;   // loads issued so far (Q tiles, K tiles)
@@ -140,23 +141,21 @@ __device__ void run_producer_v(const Ctx& c, const PrefillParams& p, const CUten
       const int s = v_g % NSTAGE;
       const uint32_t use = v_g / NSTAGE;
       if (use > 0 && !c.wait(VE + s, (use - 1) & 1)) { ok = false; break; }
-      mbar_arrive_expect_tx(c.bar(PV + s), V_PANELS * PANEL);
+      mbar_arrive_expect_tx(c.bar(VF + s), V_PANELS * PANEL);
       for (int i = 0; i < V_PANELS; ++i)
-        tma_load_3d(c.sbase + OFF_V + (s * V_PANELS + i) * PANEL, tv, c.bar(PV + s), i * 64, u.head, row);
+        tma_load_3d(c.sbase + OFF_V + (s * V_PANELS + i) * PANEL, tv, c.bar(VF + s), i * 64, u.head, row);
       ++v_g;
     }
   }
-  // The last phase of a PV barrier also needs the softmax warps' arrivals, which come on
-  // the normal path; after an abort this gives up at the drain limit.
   for (int s = 0; s < NSTAGE; ++s)
-    if (v_g > s) c.drain(PV + s, (((v_g - 1 - s) / NSTAGE)) & 1);
+    if (v_g > s) c.drain(VF + s, (((v_g - 1 - s) / NSTAGE)) & 1);
 }
 
 // ------------------------------------------------------------------ MMA issuer
 // Two MMA issuers.  A tcgen05.mma issue returns only once the tensor pipe takes the
 // instruction, so every wait of an issuing thread leaves the pipe idle unless another
 // thread has products queued: warp 1 issues S = Q K^T, warp 11 issues O += P V, and
-// each one's waits hide behind the other's products.  S of tile g + 2 reuses the S
+// each one's waits hide behind the other's products.  S of tile g + 3 reuses the S
 // buffer whose P the product of tile g reads, which the SE barrier orders.
 __device__ void run_mma_qk(const Ctx& c, const PrefillParams& p, uint32_t tmem, int ubeg, int uend) {
   int q_g = 0, kv_g = 0;
@@ -171,9 +170,9 @@ __device__ void run_mma_qk(const Ctx& c, const PrefillParams& p, uint32_t tmem, 
     if (!c.wait(QF, q_g & 1)) { ok = false; break; }
     ++q_g;
     for (int j = 0; j < n && ok; ++j) {
-      const int g = kv_g + j, s = g % NSTAGE, b = g & 1;
+      const int g = kv_g + j, s = g % NSTAGE, b = g % NSB;
       if (!c.wait(KF + s, (g / NSTAGE) & 1)) { ok = false; break; }
-      if (g >= 2 && !c.wait(SE + b, ((g - 2) >> 1) & 1)) { ok = false; break; }
+      if (g >= NSB && !c.wait(SE + b, ((g - NSB) / NSB) & 1)) { ok = false; break; }
       tc_fence_after();
       const uint64_t kd = k_desc0 + (uint64_t)(s * K_PANELS * PANEL >> 4);
 #pragma unroll
@@ -201,10 +200,9 @@ __device__ void run_mma_pv(const Ctx& c, const PrefillParams& p, uint32_t tmem, 
     const int lo = u.kv_tiles & 0xFFFF, hi = (u.kv_tiles >> 16) & 0xFFFF;
     const int n = hi - lo;
     for (int j = 0; j < n; ++j, ++g) {
-      // Tiles are counted alike for S buffers and V stages (both advance once per
-      // tile), so one barrier per parity covers "P written" and "V landed".
-      const int b = g & 1, s = g % NSTAGE;
-      if (!c.wait(PV + b, (g >> 1) & 1)) { ok = false; break; }
+      // Tiles are counted alike for S buffers and V stages (both advance once per tile).
+      const int b = g % NSB, s = g % NSTAGE;
+      if (!c.wait(PR + b, (g / NSB) & 1) || !c.wait(VF + s, (g / NSTAGE) & 1)) { ok = false; break; }
       tc_fence_after();
       const uint64_t vd = v_desc0 + (uint64_t)(s * V_PANELS * PANEL >> 4);
 #pragma unroll
@@ -260,8 +258,8 @@ __device__ void run_softmax(const Ctx& c, const PrefillParams& p, uint32_t tmem,
     const int klo = p.window_left >= 0 ? max(0, qpos + u.diag - p.window_left) : 0;
     float m_used = NEG_INF, l = 0.f;          // running max (log2 units) and this half's sum
     for (int j = 0; j < n; ++j) {
-      const int sg = s_g + j, b = sg & 1;
-      if (!__all_sync(0xffffffffu, c.wait(SF + b, (sg >> 1) & 1))) { ok = false; break; }
+      const int sg = s_g + j, b = sg % NSB, xb = sg & 1;
+      if (!__all_sync(0xffffffffu, c.wait(SF + b, (sg / NSB) & 1))) { ok = false; break; }
       tc_fence_after();
       float sv[64];
       tmem_ld64_sync(lane_addr + TM_S(b) + half * 64, reinterpret_cast<uint32_t*>(sv));
@@ -284,8 +282,8 @@ __device__ void run_softmax(const Ctx& c, const PrefillParams& p, uint32_t tmem,
                       fmaxf(sv[8 * k + 6], sv[8 * k + 7]));
       float m_half = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
       xmax[((sg & 1) * 2 + half) * 128 + row] = m_half;
-      mbar_arrive(c.bar(XM + b));
-      if (!__all_sync(0xffffffffu, c.wait(XM + b, (sg >> 1) & 1))) { ok = false; break; }
+      mbar_arrive(c.bar(XM + xb));
+      if (!__all_sync(0xffffffffu, c.wait(XM + xb, (sg >> 1) & 1))) { ok = false; break; }
       const float m_raw = fmaxf(m_half, xmax[((sg & 1) * 2 + (half ^ 1)) * 128 + row]);
       const float mt = m_raw * sc2.x;       // tile max in log2 units (-inf stays -inf)
       float m_new = m_used;
@@ -336,7 +334,7 @@ __device__ void run_softmax(const Ctx& c, const PrefillParams& p, uint32_t tmem,
       m_used = m_new;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(PV + b));
+      if (lane == 0) mbar_arrive(c.bar(PR + b));
     }
     if (!ok) break;
     if (!__all_sync(0xffffffffu, c.wait(OD, od_g & 1))) { ok = false; break; }
@@ -392,8 +390,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     for (int i = 0; i < NBAR; ++i) mbar_init(c.bar(i), 1);
     const int softmax_bars[3] = {XM + 0, XM + 1, XL};
     for (int i = 0; i < 3; ++i) mbar_init(c.bar(softmax_bars[i]), 256);
-    mbar_init(c.bar(PV + 0), 9);   // 8 softmax warps + the V producer's expect_tx arrival
-    mbar_init(c.bar(PV + 1), 9);
+    for (int i = 0; i < NSB; ++i) mbar_init(c.bar(PR + i), 8);   // one arrival per softmax warp
     *abort_flag = 0;
     fence_barrier_init();
   }
