@@ -144,14 +144,21 @@ def test_cache_write_then_gather_round_trip():
 
 
 # ------------------------------------------------------------------ up-projection
-@pytest.mark.parametrize("tokens,heads", [(300, 4), (128, 1), (1, 2), (1000, 16)])
-def test_up_proj_matches_rounded_oracle(tokens, heads):
+@pytest.mark.parametrize("tokens,heads,out_offset", [(300, 4, 0), (128, 1, 0), (1, 2, 0), (1000, 16, 0),
+                                                     (300, 4, 8), (77, 3, 8)])
+def test_up_proj_matches_rounded_oracle(tokens, heads, out_offset):
+    """out_offset = 8 elements puts K and V 16 but not 32 bytes into their buffers (16-byte stores)."""
     mla = _mla()
     rng = np.random.default_rng(tokens + heads)
     lat = wl.to_bf16_bits(rng.standard_normal((tokens, 576)).astype(np.float32))
     w = wl.to_bf16_bits((rng.standard_normal((512, heads * 256)) * 512 ** -0.5).astype(np.float32))
-    k, v = mla.mla_up_proj(to_dev_bf16(lat), to_dev_bf16(w), heads)
+    k_buf = torch.full((out_offset + tokens * heads * 192,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    v_buf = torch.full((out_offset + tokens * heads * 128,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    k_out = k_buf[out_offset:].view(tokens, heads, 192)
+    v_out = v_buf[out_offset:].view(tokens, heads, 128)
+    k, v = mla.mla_up_proj(to_dev_bf16(lat), to_dev_bf16(w), heads, k_out=k_out, v_out=v_out)
     torch.cuda.synchronize()
+    assert bool(torch.isnan(k_buf[:out_offset]).all()) and bool(torch.isnan(v_buf[:out_offset]).all())
     k_ref, v_ref = up_project(lat, w, heads)
     # Worst-case fp32 accumulation error of a 512-term dot product, per output element.
     a = np.abs(bf16_bits_to_f64(lat[:, :512]))
