@@ -348,25 +348,50 @@ __device__ void run_softmax(const Ctx& c, const PrefillParams& p, uint32_t tmem,
     if (!__all_sync(0xffffffffu, c.wait(XL, xl_g & 1))) { ok = false; break; }
     ++xl_g;
     const float l_row = l + xsum[(half ^ 1) * 128 + row];
-    if (row_ok) {
+    {
       const bool empty = !(l_row > 0.f);
       const float inv = empty ? 0.f : 1.f / l_row;
-      uint32_t w[32];
+      uint32_t w[4][8];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(ov[2 * i] * inv, ov[2 * i + 1] * inv);
-      // This thread's 64 values are 128 contiguous bytes of its row.  Neighbouring lanes
-      // hold rows num_heads * 256 bytes apart, so each store instruction touches 32 rows:
-      // 32-byte stores write whole sectors and halve the instructions.
-      char* dstb = reinterpret_cast<char*>(p.o + orow * 128 + half * 64);
-      if (p.o_align32) {
+      for (int q = 0; q < 4; ++q)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) st_global_v8(dstb + q * 32, w + 8 * q);
-      } else {
+        for (int e = 0; e < 8; ++e) w[q][e] = pack_bf16x2(ov[16 * q + 2 * e] * inv, ov[16 * q + 2 * e + 1] * inv);
+      // Lanes 4g..4g+3 hold rows 4g..4g+3.  A 4 x 4 exchange of 32-byte pieces (at each
+      // stage, lanes whose bit m differs swap the pieces whose bit m differs from their
+      // own) leaves lane 4g+jj with piece jj of all four rows, so each warp store writes
+      // 8 whole 128-byte row segments instead of touching 32 rows.
+      const int jj = lane & 3;
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          reinterpret_cast<uint4*>(dstb)[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+      for (int m = 2; m >= 1; m >>= 1) {
+        const bool hi = (jj & m) != 0;
+#pragma unroll
+        for (int q0 = 0; q0 < 4; ++q0) {
+          if (q0 & m) continue;
+          const int q1 = q0 | m;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const uint32_t send = hi ? w[q0][e] : w[q1][e];
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, m);
+            w[q0][e] = hi ? recv : w[q0][e];
+            w[q1][e] = hi ? w[q1][e] : recv;
+          }
+        }
       }
-      if (p.lse && half == 0) {
+      const int r0 = row - jj;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (r0 + i < u.q_rows) {
+          char* dstb = reinterpret_cast<char*>(p.o + ((size_t)(u.q_row0 + r0 + i) * p.num_heads + u.head) * 128 +
+                                               half * 64) + jj * 32;
+          if (p.o_align32) {
+            st_global_v8(dstb, w[i]);
+          } else {
+            reinterpret_cast<uint4*>(dstb)[0] = make_uint4(w[i][0], w[i][1], w[i][2], w[i][3]);
+            reinterpret_cast<uint4*>(dstb)[1] = make_uint4(w[i][4], w[i][5], w[i][6], w[i][7]);
+          }
+        }
+      }
+      if (row_ok && p.lse && half == 0) {
         float lg;
         asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(l_row));
         p.lse[orow] = empty ? NEG_INF : (m_used + lg) * 0.6931471805599453f;
