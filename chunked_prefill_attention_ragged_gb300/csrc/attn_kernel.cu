@@ -6,18 +6,22 @@
 // causal for new tokens / non-causal for prefix chunks, sm_scale, window_left,
 // logits_soft_cap; FlashInferPrefillImpl.run_prefill_*: O and LSE per (row, head)).
 //
-// Design (one persistent CTA per SM, one work unit = 128 query rows of one head):
-//   warps 0, 10 TMA producers: warp 0 loads the Q tile once per unit and K tiles of 128
-//               keys, warp 10 V tiles, each through a two-stage ring.
-//   warps 1, 11 MMA issuers (one thread each): warp 1 issues S = Q K^T into one of three
+// Design (one persistent CTA per SM, one work unit = 128 query rows of one head; four
+// warpgroups, registers moved between them with setmaxnreg):
+//   warps 0, 2  TMA producers: warp 0 loads the Q tile once per unit and K tiles of 128
+//               keys, warp 2 V tiles, each through a two-stage ring.
+//   warps 1, 3  MMA issuers (one thread each): warp 1 issues S = Q K^T into one of three
 //               TMEM S buffers (tcgen05.mma, both operands from shared memory), so S
-//               runs up to two tiles ahead of the softmax; warp 11 issues O += P V with
+//               runs up to two tiles ahead of the softmax; warp 3 issues O += P V with
 //               P read from TMEM (written there by the softmax warps over the S buffer).
-//   warps 2-9   softmax: two threads per query row (= one TMEM lane), each owning 64
+//   warps 4-11  softmax: two threads per query row (= one TMEM lane), each owning 64
 //               of the tile's 128 key columns and 64 of O's 128 columns.  Online
 //               softmax in base 2; O in TMEM is rescaled only when the running max
-//               grows by more than 2^8, so most tiles need no correction pass.
-//               Epilogue normalises O, writes it (bf16) and the natural-log LSE (fp32).
+//               grows by more than 2^8, so most tiles need no correction pass.  At the
+//               end of a unit they only publish each row's sum and max and go on.
+//   warps 12-15 epilogue: read O from TMEM once the unit's last P V is done, release
+//               it for the next unit's first P V, then normalise, write O (bf16) and
+//               the natural-log LSE (fp32), off the softmax warps' critical path.
 // TMEM: S buffers 0-2 (128 columns each; P overwrites the front of its S as bf16), O.
 // Every pipeline wait is bounded: on time-out the CTA records MLA_DEVSTAT_TIMEOUT,
 // drains its own copies and MMAs, frees TMEM and returns.
@@ -48,18 +52,34 @@ enum Bar {
   VF = 6,               // [stage] V tile landed
   VE = 8,               // [stage] V tile released
   SF = 10,              // [S buffer] S = Q K^T done
-  OD = 13,              // O += P V done
-  SE = 14,              // [S buffer] P V done reading P: S may be overwritten
-  FINQ = 17, FINP = 18, // all MMAs of each issuer drained before TMEM is released
-  XM = 19, XL = 21,     // softmax half-row exchanges (max per tile, sum per unit)
+  SE = 13,              // [S buffer] P V done reading P: S may be overwritten
+  OD = 16,              // [tile parity] O += P V done
+  FINQ = 18, FINP = 19, // all MMAs of each issuer drained before TMEM is released
+  XM = 20,              // [tile parity] softmax half-row max exchange
   PR = 22,              // [S buffer] P written by all 8 softmax warps
-  NBAR = 25
+  LR = 25,              // [unit parity] row sums and max of a unit published
+  LFR = 27,             // [unit parity] the epilogue has read them
+  OFR = 29,             // the epilogue has read O: the next unit's first P V may overwrite it
+  NBAR = 30
 };
-constexpr int OFF_XCHG = OFF_BAR + NBAR * 8;      // row-max / row-sum exchange, 6 x 128 floats
-constexpr int OFF_MISC = OFF_XCHG + 6 * 128 * 4;
+// Parity waits: a wait for phase f of a barrier is exact only while phase f - 1 has
+// completed and phase f + 1 cannot have.  O-done is split by tile parity so that the
+// softmax (which skips each unit's last product) and the epilogue (which waits only for
+// it) both meet that: products complete in order, P(g - 3) V has completed whenever S(g)
+// exists, and P(g + 1) V needs a P (or the epilogue's release of O) not yet given.
+// Exchange area: row max per (tile parity, half) and, per unit parity, both halves'
+// row sums and the row max, 10 x 128 floats.
+constexpr int OFF_XCHG = OFF_BAR + NBAR * 8;
+constexpr int OFF_MISC = OFF_XCHG + 10 * 128 * 4;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + slack for 1024-byte alignment
 
-constexpr int NTHREADS = 384;   // Q/K producer, S issuer, 8 softmax warps, V producer, O issuer
+constexpr int NTHREADS = 512;   // 4 warpgroups: control, softmax x 2, epilogue
+// Registers per thread: launched at 65536 / 512 = 128; the control and epilogue
+// warpgroups give some up and the two softmax warpgroups take them (the smallest counts
+// at which no role spills).
+constexpr int LAUNCH_REGS = 128, CTRL_REGS = 88, SOFTMAX_REGS = 160, EPI_REGS = 104;
+static_assert(4 * 32 * (CTRL_REGS + 2 * SOFTMAX_REGS + EPI_REGS) <= 4 * 32 * 4 * LAUNCH_REGS,
+              "register split exceeds the launch allocation");
 constexpr uint32_t TMEM_COLS = 512;
 __device__ __forceinline__ constexpr uint32_t TM_S(int b) { return (uint32_t)b * 128u; }
 constexpr uint32_t TM_O = 384;
@@ -96,7 +116,7 @@ __device__ __forceinline__ Unit load_unit(const Unit* units, int i) {
 
 // ------------------------------------------------------------------ producers
 // Two producer threads, so that a K load never queues behind a V load waiting for its
-// stage: warp 0 loads Q (once per unit) and K tiles, warp 10 loads V tiles.  A K stage
+// stage: warp 0 loads Q (once per unit) and K tiles, warp 2 loads V tiles.  A K stage
 // frees when its S = Q K^T is done, a V stage when its P V is done.
 __device__ void run_producer_qk(const Ctx& c, const PrefillParams& p, const CUtensorMap* tq,
                                 const CUtensorMap* tk, int ubeg, int uend) {
@@ -154,7 +174,7 @@ __device__ void run_producer_v(const Ctx& c, const PrefillParams& p, const CUten
 // ------------------------------------------------------------------ MMA issuer
 // Two MMA issuers.  A tcgen05.mma issue returns only once the tensor pipe takes the
 // instruction, so every wait of an issuing thread leaves the pipe idle unless another
-// thread has products queued: warp 1 issues S = Q K^T, warp 11 issues O += P V, and
+// thread has products queued: warp 1 issues S = Q K^T, warp 3 issues O += P V, and
 // each one's waits hide behind the other's products.  S of tile g + 3 reuses the S
 // buffer whose P the product of tile g reads, which the SE barrier orders.
 __device__ void run_mma_qk(const Ctx& c, const PrefillParams& p, uint32_t tmem, int ubeg, int uend) {
@@ -192,13 +212,18 @@ __device__ void run_mma_qk(const Ctx& c, const PrefillParams& p, uint32_t tmem, 
 }
 
 __device__ void run_mma_pv(const Ctx& c, const PrefillParams& p, uint32_t tmem, int ubeg, int uend) {
-  int g = 0;
+  int g = 0, k = 0;   // tiles and non-empty units so far
   bool ok = true;
   const uint64_t v_desc0 = sdesc_sw128(c.sbase + OFF_V, PANEL, 1024);
   for (int ui = ubeg; ui < uend && ok; ++ui) {
     const Unit u = load_unit(p.units, ui);
     const int lo = u.kv_tiles & 0xFFFF, hi = (u.kv_tiles >> 16) & 0xFFFF;
     const int n = hi - lo;
+    if (n <= 0) continue;
+    // The first product of a unit overwrites O: the epilogue must have read the
+    // previous unit's O out of TMEM.
+    if (k > 0 && !c.wait(OFR, (k - 1) & 1)) { ok = false; break; }
+    ++k;
     for (int j = 0; j < n; ++j, ++g) {
       // Tiles are counted alike for S buffers and V stages (both advance once per tile).
       const int b = g % NSB, s = g % NSTAGE;
@@ -211,7 +236,7 @@ __device__ void run_mma_pv(const Ctx& c, const PrefillParams& p, uint32_t tmem, 
                (j > 0 || kk > 0) ? 1u : 0u);
       tc_commit(c.bar(VE + s));
       tc_commit(c.bar(SE + b));
-      tc_commit(c.bar(OD));
+      tc_commit(c.bar(OD + (g & 1)));
     }
   }
   tc_commit(c.bar(FINP));
@@ -219,21 +244,21 @@ __device__ void run_mma_pv(const Ctx& c, const PrefillParams& p, uint32_t tmem, 
 }
 
 // ------------------------------------------------------------------ softmax
-// Two threads per query row: warps 2-5 own key columns 0-63 of every tile, warps 6-9
+// Two threads per query row: warps 4-7 own key columns 0-63 of every tile, warps 8-11
 // columns 64-127 (a warp may only touch TMEM lanes 32*(warp%4)..+31, so both halves cover
-// all 128 rows).  The halves agree on the row max through shared memory once per tile,
-// and on the row sum once per unit; both exchanges sit behind mbarriers so every wait
-// stays bounded.
+// all 128 rows).  The halves agree on the row max through shared memory once per tile;
+// at the end of a unit each publishes its row sum (and half 0 the row max) for the
+// epilogue warps.  Every exchange sits behind an mbarrier so every wait stays bounded.
 __device__ void run_softmax(const Ctx& c, const PrefillParams& p, uint32_t tmem, float* xchg,
                             int ubeg, int uend) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;                 // TMEM lanes this warp may touch
-  const int half = (warp - 2) >> 2;          // 0: key columns 0-63, 1: 64-127
+  const int half = (warp - 4) >> 2;          // 0: key columns 0-63, 1: 64-127
   const int row = quad * 32 + lane;
   const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
   float* xmax = xchg;                        // [2 parity][2 half][128 rows]
-  float* xsum = xchg + 4 * 128;              // [2 half][128 rows]
-  int s_g = 0, od_g = 0, xl_g = 0;
+  float* xlm = xchg + 4 * 128;               // [2 unit parity][sum half 0, sum half 1, max][128 rows]
+  int s_g = 0, k = 0;                        // tiles and non-empty units so far
   bool ok = true;
   const float NEG_INF = -__int_as_float(0x7f800000);
   const float2 sc2 = make_float2(p.has_cap ? 1.f : p.scale_log2, p.has_cap ? 1.f : p.scale_log2);
@@ -241,11 +266,10 @@ __device__ void run_softmax(const Ctx& c, const PrefillParams& p, uint32_t tmem,
     const Unit u = load_unit(p.units, ui);
     const int lo = u.kv_tiles & 0xFFFF, hi = (u.kv_tiles >> 16) & 0xFFFF;
     const int n = hi - lo;
-    const bool row_ok = row < u.q_rows;
     const int qpos = u.q_pos0 + row;
-    const size_t orow = (size_t)(u.q_row0 + row) * p.num_heads + u.head;
     if (n <= 0) {
-      if (row_ok) {
+      const size_t orow = (size_t)(u.q_row0 + row) * p.num_heads + u.head;
+      if (row < u.q_rows) {
         uint4* dst = reinterpret_cast<uint4*>(p.o + orow * 128 + half * 64);
 #pragma unroll
         for (int i = 0; i < 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
@@ -310,9 +334,10 @@ __device__ void run_softmax(const Ctx& c, const PrefillParams& p, uint32_t tmem,
       tmem_st32_sync(lane_addr + TM_S(b) + half * 32, pr);
       float alpha = 1.f;
       if (j > 0) {
-        // O must hold P_{j-1} V_{j-1} before it may be rescaled.
-        if (!__all_sync(0xffffffffu, c.wait(OD, od_g & 1))) { ok = false; break; }
-        ++od_g;
+        // O must hold P_{j-1} V_{j-1} before it may be rescaled (tiles and products are
+        // counted alike: that product is tile sg - 1).
+        const int pg = sg - 1;
+        if (!__all_sync(0xffffffffu, c.wait(OD + (pg & 1), (pg >> 1) & 1))) { ok = false; break; }
         tc_fence_after();
         if (rescale) alpha = ex2_approx(m_used - m_new);
         // tcgen05.ld/st are warp-collective (.sync.aligned): the whole warp rescales
@@ -337,67 +362,110 @@ __device__ void run_softmax(const Ctx& c, const PrefillParams& p, uint32_t tmem,
       if (lane == 0) mbar_arrive(c.bar(PR + b));
     }
     if (!ok) break;
-    if (!__all_sync(0xffffffffu, c.wait(OD, od_g & 1))) { ok = false; break; }
-    ++od_g;
+    // Hand the unit to the epilogue warps: this half's row sum and the row max.  The
+    // slot of this unit's parity is free once the epilogue has read unit k - 2.
+    const int slot = k & 1;
+    if (k >= 2 && !__all_sync(0xffffffffu, c.wait(LFR + slot, ((k >> 1) - 1) & 1))) { ok = false; break; }
+    xlm[(slot * 3 + half) * 128 + row] = l;
+    if (half == 0) xlm[(slot * 3 + 2) * 128 + row] = m_used;
+    mbar_arrive(c.bar(LR + slot));
+    ++k;
+    s_g += n;
+  }
+}
+
+// ------------------------------------------------------------------ register split
+// Whole warpgroups (4 consecutive warps) change their per-thread register count.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// ------------------------------------------------------------------ epilogue
+// 64 columns of O, scaled by 1/l and rounded to bf16: w[q] = columns 16q .. 16q+15.
+__device__ __forceinline__ void load_scaled_half(uint32_t lane_addr, float inv, uint32_t (&w)[4][8]) {
+  const float2 inv2 = make_float2(inv, inv);
+#pragma unroll
+  for (int hq = 0; hq < 2; ++hq) {   // 32 columns at a time keeps the peak register count low
+    float ov[32];
+    tmem_ld32_sync(lane_addr + hq * 32, reinterpret_cast<uint32_t*>(ov));
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float2 x = fmul2(make_float2(ov[16 * q + 2 * e], ov[16 * q + 2 * e + 1]), inv2);
+        w[2 * hq + q][e] = pack_bf16x2(x.x, x.y);
+      }
+  }
+}
+
+// Warps 12-15, one per TMEM lane quadrant, one thread per query row and all 128 columns
+// of O.  Per unit: wait for the softmax's row sums and max, then for the unit's last
+// P V; read O, release it to the P V issuer, and store.  The stores are row per thread
+// (eight 32-byte stores of 256 contiguous bytes): off the softmax's critical path, a
+// shuffle exchange that would coalesce them costs more issue slots than it saves.
+__device__ void run_epilogue(const Ctx& c, const PrefillParams& p, uint32_t tmem, const float* xchg,
+                             int ubeg, int uend) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quad = warp & 3;
+  const int row = quad * 32 + lane;
+  const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
+  const float* xlm = xchg + 4 * 128;
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  int g = 0, k = 0;   // tiles and non-empty units so far
+  for (int ui = ubeg; ui < uend; ++ui) {
+    const Unit u = load_unit(p.units, ui);
+    const int lo = u.kv_tiles & 0xFFFF, hi = (u.kv_tiles >> 16) & 0xFFFF;
+    const int n = hi - lo;
+    if (n <= 0) continue;
+    const int slot = k & 1;
+    if (!__all_sync(0xffffffffu, c.wait(LR + slot, (k >> 1) & 1))) break;
+    const float l_row = xlm[(slot * 3 + 0) * 128 + row] + xlm[(slot * 3 + 1) * 128 + row];
+    const float m_row = xlm[(slot * 3 + 2) * 128 + row];
+    mbar_arrive(c.bar(LFR + slot));
+    // The unit's last product.  The one before it on the same barrier (tile gl - 2) has
+    // completed: the softmax waited for tile gl - 1 (n > 1) or this warp did (n = 1).
+    const int gl = g + n - 1;
+    if (!__all_sync(0xffffffffu, c.wait(OD + (gl & 1), (gl >> 1) & 1))) break;
     tc_fence_after();
-    float ov[64];
-    tmem_ld64_sync(lane_addr + TM_O + half * 64, reinterpret_cast<uint32_t*>(ov));
+    const bool empty = !(l_row > 0.f);
+    const float inv = empty ? 0.f : 1.f / l_row;
+    uint32_t w0[4][8], w1[4][8];
+    load_scaled_half(lane_addr + TM_O, inv, w0);
+    load_scaled_half(lane_addr + TM_O + 64, inv, w1);
     tc_fence_before();
-    xsum[half * 128 + row] = l;
-    mbar_arrive(c.bar(XL));
-    if (!__all_sync(0xffffffffu, c.wait(XL, xl_g & 1))) { ok = false; break; }
-    ++xl_g;
-    const float l_row = l + xsum[(half ^ 1) * 128 + row];
-    {
-      const bool empty = !(l_row > 0.f);
-      const float inv = empty ? 0.f : 1.f / l_row;
-      uint32_t w[4][8];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(c.bar(OFR));
+    if (row < u.q_rows) {
+      // Row per thread: 256 contiguous bytes, eight 32-byte stores (whole sectors).
+      char* dst = reinterpret_cast<char*>(p.o + ((size_t)(u.q_row0 + row) * p.num_heads + u.head) * 128);
+      if (p.o_align32) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) w[q][e] = pack_bf16x2(ov[16 * q + 2 * e] * inv, ov[16 * q + 2 * e + 1] * inv);
-      // Lanes 4g..4g+3 hold rows 4g..4g+3.  A 4 x 4 exchange of 32-byte pieces (at each
-      // stage, lanes whose bit m differs swap the pieces whose bit m differs from their
-      // own) leaves lane 4g+jj with piece jj of all four rows, so each warp store writes
-      // 8 whole 128-byte row segments instead of touching 32 rows.
-      const int jj = lane & 3;
-#pragma unroll
-      for (int m = 2; m >= 1; m >>= 1) {
-        const bool hi = (jj & m) != 0;
-#pragma unroll
-        for (int q0 = 0; q0 < 4; ++q0) {
-          if (q0 & m) continue;
-          const int q1 = q0 | m;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const uint32_t send = hi ? w[q0][e] : w[q1][e];
-            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, m);
-            w[q0][e] = hi ? recv : w[q0][e];
-            w[q1][e] = hi ? w[q1][e] : recv;
-          }
+        for (int q = 0; q < 4; ++q) {
+          st_global_v8(dst + q * 32, w0[q]);
+          st_global_v8(dst + 128 + q * 32, w1[q]);
         }
-      }
-      const int r0 = row - jj;
+      } else {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (r0 + i < u.q_rows) {
-          char* dstb = reinterpret_cast<char*>(p.o + ((size_t)(u.q_row0 + r0 + i) * p.num_heads + u.head) * 128 +
-                                               half * 64) + jj * 32;
-          if (p.o_align32) {
-            st_global_v8(dstb, w[i]);
-          } else {
-            reinterpret_cast<uint4*>(dstb)[0] = make_uint4(w[i][0], w[i][1], w[i][2], w[i][3]);
-            reinterpret_cast<uint4*>(dstb)[1] = make_uint4(w[i][4], w[i][5], w[i][6], w[i][7]);
-          }
+        for (int q = 0; q < 4; ++q) {
+          reinterpret_cast<uint4*>(dst + q * 32)[0] = make_uint4(w0[q][0], w0[q][1], w0[q][2], w0[q][3]);
+          reinterpret_cast<uint4*>(dst + q * 32)[1] = make_uint4(w0[q][4], w0[q][5], w0[q][6], w0[q][7]);
+          reinterpret_cast<uint4*>(dst + 128 + q * 32)[0] = make_uint4(w1[q][0], w1[q][1], w1[q][2], w1[q][3]);
+          reinterpret_cast<uint4*>(dst + 128 + q * 32)[1] = make_uint4(w1[q][4], w1[q][5], w1[q][6], w1[q][7]);
         }
-      }
-      if (row_ok && p.lse && half == 0) {
-        float lg;
-        asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(l_row));
-        p.lse[orow] = empty ? NEG_INF : (m_used + lg) * 0.6931471805599453f;
       }
     }
-    s_g += n;
+    if (p.lse && row < u.q_rows) {
+      float lg;
+      asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(l_row));
+      p.lse[(size_t)(u.q_row0 + row) * p.num_heads + u.head] = empty ? NEG_INF : (m_row + lg) * 0.6931471805599453f;
+    }
+    g += n;
+    ++k;
   }
 }
 
@@ -413,9 +481,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBAR; ++i) mbar_init(c.bar(i), 1);
-    const int softmax_bars[3] = {XM + 0, XM + 1, XL};
-    for (int i = 0; i < 3; ++i) mbar_init(c.bar(softmax_bars[i]), 256);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(c.bar(XM + i), 256);   // every softmax thread
+      mbar_init(c.bar(LR + i), 256);
+      mbar_init(c.bar(LFR + i), 128);  // every epilogue thread
+    }
     for (int i = 0; i < NSB; ++i) mbar_init(c.bar(PR + i), 8);   // one arrival per softmax warp
+    mbar_init(c.bar(OFR), 4);                                      // one arrival per epilogue warp
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -434,16 +506,21 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   const uint32_t tmem = *tmem_slot;
   const int ubeg = p.cta_offsets[blockIdx.x], uend = p.cta_offsets[blockIdx.x + 1];
 
-  if (warp == 0) {
-    if (lane == 0) run_producer_qk(c, p, &tm_q, &tm_k, ubeg, uend);
-  } else if (warp == 1) {
-    if (lane == 0) run_mma_qk(c, p, tmem, ubeg, uend);
-  } else if (warp == 10) {
-    if (lane == 0) run_producer_v(c, p, &tm_v, ubeg, uend);
-  } else if (warp == 11) {
-    if (lane == 0) run_mma_pv(c, p, tmem, ubeg, uend);
+  float* xchg = reinterpret_cast<float*>(smem + OFF_XCHG);
+  if (warp < 4) {
+    setmaxnreg_dec<CTRL_REGS>();
+    if (lane == 0) {
+      if (warp == 0) run_producer_qk(c, p, &tm_q, &tm_k, ubeg, uend);
+      else if (warp == 1) run_mma_qk(c, p, tmem, ubeg, uend);
+      else if (warp == 2) run_producer_v(c, p, &tm_v, ubeg, uend);
+      else run_mma_pv(c, p, tmem, ubeg, uend);
+    }
+  } else if (warp < 12) {
+    setmaxnreg_inc<SOFTMAX_REGS>();
+    run_softmax(c, p, tmem, xchg, ubeg, uend);
   } else {
-    run_softmax(c, p, tmem, reinterpret_cast<float*>(smem + OFF_XCHG), ubeg, uend);
+    setmaxnreg_dec<EPI_REGS>();
+    run_epilogue(c, p, tmem, xchg, ubeg, uend);
   }
   tc_fence_before();
   __syncthreads();
@@ -467,6 +544,12 @@ cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const C
   if (configured_device != dev) {
     e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
+    // The warpgroups' setmaxnreg split assumes every thread starts with LAUNCH_REGS
+    // registers; with fewer, the softmax warpgroups' increase could never be granted.
+    cudaFuncAttributes attr;
+    e = cudaFuncGetAttributes(&attr, prefill_kernel);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs != LAUNCH_REGS) return cudaErrorInvalidConfiguration;
     configured_device = dev;
   }
   prefill_kernel<<<num_ctas, NTHREADS, SMEM_BYTES, stream>>>(tq, tk, tv, p);

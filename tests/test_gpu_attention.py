@@ -101,6 +101,41 @@ def test_repeat_runs_bitwise_identical():
     assert torch.equal(l1, l2)
 
 
+def _trend_batch(q_lens, kv_lens, heads, causal, slope, seed):
+    """Q and K share a common direction whose weight in K changes by `slope` logits per key
+    (natural units) along each request, plus noise: with slope > 0 a row's running max
+    grows by ~slope * 128 per key tile, far past the 2^8 rescale threshold, so the O
+    rescale runs on every tile; with slope < 0 the first tile holds the max throughout."""
+    rng = np.random.default_rng(seed)
+    b = wl.random_ragged(seed, q_lens, kv_lens, heads, causal=causal, name="trend")
+    q = 1.0 + 0.3 * rng.standard_normal(b.q.shape)
+    k = 0.3 * rng.standard_normal(b.k.shape)
+    per_key = slope / (b.sm_scale * 192.0)          # logit change per key for q ~ ones
+    for r in range(b.batch):
+        lo, hi = int(b.kv_indptr[r]), int(b.kv_indptr[r + 1])
+        pos = np.arange(hi - lo, dtype=np.float64)
+        w = per_key * (pos if slope > 0 else pos - (hi - lo))
+        k[lo:hi] += w[:, None, None]
+    b.q = wl.to_bf16_bits(q.astype(np.float32))
+    b.k = wl.to_bf16_bits(k.astype(np.float32))
+    return b
+
+
+@pytest.mark.parametrize("q_lens,kv_lens,causal,slope", [
+    ([520, 300], None, True, 0.06),
+    ([520, 300], None, True, -0.06),
+    ([200, 70], [900, 260], False, 0.05),
+    ([130], [700], True, 0.2),
+], ids=["causal_rising", "causal_falling", "noncausal_rising", "prefix_steep"])
+def test_running_max_rescale_paths(q_lens, kv_lens, causal, slope):
+    b = _trend_batch(q_lens, kv_lens, 2, causal, slope, seed=len(q_lens) + int(abs(slope) * 100))
+    _, _, o, lse = run_gpu(b)
+    o_ref, lse_ref = oracle(b)
+    # The logits really do span many rescale thresholds.
+    assert np.nanmax(lse_ref) - np.nanmin(lse_ref) > 12.0
+    check_attention(f64_of_bf16(o), lse.double().cpu().numpy(), o_ref, lse_ref, f"trend {slope}")
+
+
 @pytest.mark.parametrize("cap", [0.0, 30.0])
 def test_workload4_many_short_full(cap):
     b = wl.make_workload(4, logits_soft_cap=cap)
