@@ -447,10 +447,11 @@ def bench_chunked(args, dev, peaks):
     pipe.check_status()
     stream = torch.cuda.current_stream(dev)
     reps = 5
-    names = ["main_attention", "gather", "up_proj", "chunk_attention", "merge"]
+    names = ["main_attention", "gather", "up_proj", "chunk_attention", "chunk_attention_unfused", "merge"]
     acc = {n: [] for n in names}
     total = []
     nC = pipe.cu.shape[0]
+    # The pipeline as it runs: each chunk's attention merges into (o, lse) in its epilogue.
     for _ in range(reps):
         flush.zero_()
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(3 + 8 * nC)]
@@ -468,20 +469,37 @@ def bench_chunked(args, dev, peaks):
             e1 = evs[i]; e1.record(stream); i += 1
             mla.mla_up_proj(lat, w, b.num_heads, kc, vc, pipe.status)
             e2 = evs[i]; e2.record(stream); i += 1
-            plan.run(q, kc, vc, pipe.o_c, pipe.lse_c)
+            plan.run_merge(q, kc, vc, o, lse)
             e3 = evs[i]; e3.record(stream); i += 1
-            mla.mla_merge_state(o, lse, pipe.o_c, pipe.lse_c, o, lse)
-            e4 = evs[i]; e4.record(stream); i += 1
-            marks.append((e1, e2, e3, e4))
+            marks.append((e1, e2, e3))
         torch.cuda.synchronize()
         acc["main_attention"].append(evs[0].elapsed_time(evs[1]))
         acc["gather"].append(evs[1].elapsed_time(evs[2]))
-        for e1, e2, e3, e4 in marks:
+        for e1, e2, e3 in marks:
             acc["up_proj"].append(e1.elapsed_time(e2))
             acc["chunk_attention"].append(e2.elapsed_time(e3))
-            acc["merge"].append(e3.elapsed_time(e4))
-        total.append(evs[0].elapsed_time(marks[-1][3]))
+        total.append(evs[0].elapsed_time(marks[-1][2]))
     pipe.check_status()
+    # The same chunk step unfused, for comparison and for the merge kernel's own row: the
+    # attention writes its O/LSE, then mla_merge_state merges them into (o, lse).
+    o_c = torch.empty_like(o)
+    lse_c = torch.empty_like(lse)
+    for _ in range(reps):
+        for c, plan in enumerate(pipe.chunks):
+            t = pipe.chunk_tokens[c]
+            kc, vc = pipe.k_c[:t], pipe.v_c[:t]
+            flush.zero_()
+            e1, e2, e3 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e1.record(stream)
+            plan.run(q, kc, vc, o_c, lse_c)
+            e2.record(stream)
+            mla.mla_merge_state(o, lse, o_c, lse_c, o, lse)
+            e3.record(stream)
+            torch.cuda.synchronize()
+            acc["chunk_attention_unfused"].append(e1.elapsed_time(e2))
+            acc["merge"].append(e2.elapsed_time(e3))
+    pipe.check_status()
+    del o_c, lse_c
     # The gather alone, from a cold and clean L2: 256 MB written, then a second 256 MB
     # buffer read, so no dirty line of earlier kernels is evicted inside the timed launch.
     flush_read = torch.ones(64 << 20, dtype=torch.int32, device=dev)
@@ -539,7 +557,11 @@ def bench_chunked(args, dev, peaks):
         "main_attention": {"ms": round(med["main_attention"], 4),
                            "tflops": round(main_f / med["main_attention"] / 1e9, 2)},
         "chunk_attention": {"ms": round(med["chunk_attention"], 4),
-                            "tflops": round(chunk_f / med["chunk_attention"] / 1e9, 2)},
+                            "tflops": round(chunk_f / med["chunk_attention"] / 1e9, 2),
+                            "merge": "fused into the attention epilogue (mla_prefill_run_merge)"},
+        "chunk_attention_unfused": {"ms": round(med["chunk_attention_unfused"], 4),
+                                    "tflops": round(chunk_f / med["chunk_attention_unfused"] / 1e9, 2),
+                                    "plus_merge_ms": round(med["merge"], 4)},
         "up_proj": {"ms": round(med["up_proj"], 4), "tflops": round(upf / med["up_proj"] / 1e9, 2),
                     "gbs": round(up_bytes / med["up_proj"] / 1e6, 1)},
         "gather": {"ms": round(med["gather"], 4), "gbs": round(gather_bytes / med["gather"] / 1e6, 1),
@@ -553,7 +575,8 @@ def bench_chunked(args, dev, peaks):
                         "frac_hbm": round(cw_bytes / statistics.median(cw) / 1e6 / hbm, 3),
                         "l2": "256 MB written, then another 256 MB read, before each launch"},
         "merge": {"ms": round(med["merge"], 4), "gbs": round(merge_bytes / med["merge"] / 1e6, 1),
-                  "frac_hbm": round(merge_bytes / med["merge"] / 1e6 / hbm, 3)},
+                  "frac_hbm": round(merge_bytes / med["merge"] / 1e6 / hbm, 3),
+                  "note": "mla_merge_state alone (the unfused step); the pipeline fuses it"},
         "hbm_peak_gbs": hbm, "hbm_peak_source": peaks["source"],
     }
 

@@ -29,6 +29,7 @@ _SIGNATURES = {
     "mla_prefill_plan": (_c_int, [ctypes.POINTER(_c_vp), _i32p, _i32p, _c_int, _c_int, _c_int, _c_int, _c_int,
                                   _c_f, _c_int, _c_f, _c_vp]),
     "mla_prefill_run": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
+    "mla_prefill_run_merge": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
     "mla_prefill_status": (_c_int, [_c_vp]),
     "mla_plan_destroy": (_c_int, [_c_vp]),
     "mla_plan_query": (_c_int, [_c_vp, _c_int, _i64p]),
@@ -136,6 +137,9 @@ class PrefillPlan:
     def run(self, q, k, v, o=None, lse=None, return_lse=True, stream=None):
         return mla_prefill_run(self, q, k, v, o, lse, return_lse, stream)
 
+    def run_merge(self, q, k, v, o, lse, stream=None):
+        return mla_prefill_run_merge(self, q, k, v, o, lse, stream)
+
     def status(self) -> int:
         return mla_prefill_status(self)
 
@@ -187,6 +191,25 @@ def mla_prefill_run(plan: PrefillPlan, q, k, v, o=None, lse=None, return_lse=Tru
     _check(library().mla_prefill_run(plan.handle, _dev(q, bf, "q"), _dev(k, bf, "k"), _dev(v, bf, "v"),
                                      _dev(o, bf, "o"), _dev(lse, torch.float32, "lse"), _stream(stream)),
            "mla_prefill_run")
+    return o, lse
+
+
+def mla_prefill_run_merge(plan: PrefillPlan, q, k, v, o, lse, stream=None):
+    """Run a plan and merge the result into the partial state (o, lse) in place; returns (o, lse)."""
+    import torch
+    H = plan.num_heads
+    if tuple(q.shape) != (plan.total_q, H, 192):
+        raise ValueError(f"q must be [{plan.total_q}, {H}, 192], got {tuple(q.shape)}")
+    if tuple(k.shape) != (plan.total_kv, H, 192) or tuple(v.shape) != (plan.total_kv, H, 128):
+        raise ValueError("k/v shapes do not match the plan")
+    if o is None or lse is None:
+        raise ValueError("mla_prefill_run_merge needs the partial state o and lse")
+    if tuple(o.shape) != (plan.total_q, H, 128) or tuple(lse.shape) != (plan.total_q, H):
+        raise ValueError("o/lse shapes do not match the plan")
+    bf = torch.bfloat16
+    _check(library().mla_prefill_run_merge(plan.handle, _dev(q, bf, "q"), _dev(k, bf, "k"), _dev(v, bf, "v"),
+                                           _dev(o, bf, "o"), _dev(lse, torch.float32, "lse"), _stream(stream)),
+           "mla_prefill_run_merge")
     return o, lse
 
 

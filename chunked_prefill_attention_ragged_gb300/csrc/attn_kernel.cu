@@ -75,11 +75,15 @@ constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + slack for 1024-byte alig
 
 constexpr int NTHREADS = 512;   // 4 warpgroups: control, softmax x 2, epilogue
 // Registers per thread: launched at 65536 / 512 = 128; the control and epilogue
-// warpgroups give some up and the two softmax warpgroups take them (the smallest counts
-// at which no role spills).
-constexpr int LAUNCH_REGS = 128, CTRL_REGS = 88, SOFTMAX_REGS = 160, EPI_REGS = 104;
-static_assert(4 * 32 * (CTRL_REGS + 2 * SOFTMAX_REGS + EPI_REGS) <= 4 * 32 * 4 * LAUNCH_REGS,
-              "register split exceeds the launch allocation");
+// warpgroups give some up and the two softmax warpgroups take them (counts at which
+// ptxas reports no spills; the merging epilogue needs a few more).
+constexpr int LAUNCH_REGS = 128;
+template <bool kMerge>
+struct RegSplit {
+  static constexpr int ctrl = kMerge ? 96 : 88, softmax = kMerge ? 152 : 160, epi = kMerge ? 112 : 104;
+  static_assert(4 * 32 * (ctrl + 2 * softmax + epi) <= 4 * 32 * 4 * LAUNCH_REGS,
+                "register split exceeds the launch allocation");
+};
 constexpr uint32_t TMEM_COLS = 512;
 __device__ __forceinline__ constexpr uint32_t TM_S(int b) { return (uint32_t)b * 128u; }
 constexpr uint32_t TM_O = 384;
@@ -249,6 +253,7 @@ __device__ void run_mma_pv(const Ctx& c, const PrefillParams& p, uint32_t tmem, 
 // all 128 rows).  The halves agree on the row max through shared memory once per tile;
 // at the end of a unit each publishes its row sum (and half 0 the row max) for the
 // epilogue warps.  Every exchange sits behind an mbarrier so every wait stays bounded.
+template <bool kMerge>
 __device__ void run_softmax(const Ctx& c, const PrefillParams& p, uint32_t tmem, float* xchg,
                             int ubeg, int uend) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -268,12 +273,15 @@ __device__ void run_softmax(const Ctx& c, const PrefillParams& p, uint32_t tmem,
     const int n = hi - lo;
     const int qpos = u.q_pos0 + row;
     if (n <= 0) {
+      // No allowed key: O = 0, LSE = -inf.  Merged into a partial state that leaves the
+      // state as it is, except that a state at LSE = -inf (no key on either side) gets
+      // O = 0 whatever its O held.
       const size_t orow = (size_t)(u.q_row0 + row) * p.num_heads + u.head;
-      if (row < u.q_rows) {
+      if (row < u.q_rows && (!kMerge || p.lse[orow] == NEG_INF)) {
         uint4* dst = reinterpret_cast<uint4*>(p.o + orow * 128 + half * 64);
 #pragma unroll
         for (int i = 0; i < 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
-        if (p.lse && half == 0) p.lse[orow] = NEG_INF;
+        if (!kMerge && p.lse && half == 0) p.lse[orow] = NEG_INF;
       }
       continue;
     }
@@ -403,11 +411,66 @@ __device__ __forceinline__ void load_scaled_half(uint32_t lane_addr, float inv, 
   }
 }
 
+// w (bf16 pairs of 64 columns) += a * the 64 bf16 columns at src (16-byte aligned), in
+// fp32, rounded back to bf16.
+__device__ __forceinline__ void merge_old(const char* src, float a, uint32_t (&w)[4][8]) {
+  const float2 a2 = make_float2(a, a);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src + q * 32);
+    const uint4 x = s4[0], y = s4[1];
+    const uint32_t old[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float2 o = make_float2(__uint_as_float(old[e] << 16), __uint_as_float(old[e] & 0xffff0000u));
+      const float2 n = make_float2(__uint_as_float(w[q][e] << 16), __uint_as_float(w[q][e] & 0xffff0000u));
+      const float2 r = ffma2(o, a2, n);
+      w[q][e] = pack_bf16x2(r.x, r.y);
+    }
+  }
+}
+
+// 64 columns of a row of O: 128 contiguous bytes, four 32-byte stores or eight 16-byte ones.
+__device__ __forceinline__ void store_half(char* dst, int align32, const uint32_t (&w)[4][8]) {
+  if (align32) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) st_global_v8(dst + q * 32, w[q]);
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      reinterpret_cast<uint4*>(dst + q * 32)[0] = make_uint4(w[q][0], w[q][1], w[q][2], w[q][3]);
+      reinterpret_cast<uint4*>(dst + q * 32)[1] = make_uint4(w[q][4], w[q][5], w[q][6], w[q][7]);
+    }
+  }
+}
+
+// One row of O: 256 contiguous bytes, eight 32-byte stores (whole sectors), or sixteen
+// 16-byte stores when O is only 16-byte aligned.
+__device__ __forceinline__ void store_row(char* dst, int align32, const uint32_t (&w0)[4][8],
+                                          const uint32_t (&w1)[4][8]) {
+  if (align32) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      st_global_v8(dst + q * 32, w0[q]);
+      st_global_v8(dst + 128 + q * 32, w1[q]);
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      reinterpret_cast<uint4*>(dst + q * 32)[0] = make_uint4(w0[q][0], w0[q][1], w0[q][2], w0[q][3]);
+      reinterpret_cast<uint4*>(dst + q * 32)[1] = make_uint4(w0[q][4], w0[q][5], w0[q][6], w0[q][7]);
+      reinterpret_cast<uint4*>(dst + 128 + q * 32)[0] = make_uint4(w1[q][0], w1[q][1], w1[q][2], w1[q][3]);
+      reinterpret_cast<uint4*>(dst + 128 + q * 32)[1] = make_uint4(w1[q][4], w1[q][5], w1[q][6], w1[q][7]);
+    }
+  }
+}
+
 // Warps 12-15, one per TMEM lane quadrant, one thread per query row and all 128 columns
 // of O.  Per unit: wait for the softmax's row sums and max, then for the unit's last
 // P V; read O, release it to the P V issuer, and store.  The stores are row per thread
 // (eight 32-byte stores of 256 contiguous bytes): off the softmax's critical path, a
 // shuffle exchange that would coalesce them costs more issue slots than it saves.
+template <bool kMerge>
 __device__ void run_epilogue(const Ctx& c, const PrefillParams& p, uint32_t tmem, const float* xchg,
                              int ubeg, int uend) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -432,43 +495,74 @@ __device__ void run_epilogue(const Ctx& c, const PrefillParams& p, uint32_t tmem
     const int gl = g + n - 1;
     if (!__all_sync(0xffffffffu, c.wait(OD + (gl & 1), (gl >> 1) & 1))) break;
     tc_fence_after();
+    const bool live = row < u.q_rows;
     const bool empty = !(l_row > 0.f);
-    const float inv = empty ? 0.f : 1.f / l_row;
-    uint32_t w0[4][8], w1[4][8];
-    load_scaled_half(lane_addr + TM_O, inv, w0);
-    load_scaled_half(lane_addr + TM_O + 64, inv, w1);
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(c.bar(OFR));
-    if (row < u.q_rows) {
-      // Row per thread: 256 contiguous bytes, eight 32-byte stores (whole sectors).
-      char* dst = reinterpret_cast<char*>(p.o + ((size_t)(u.q_row0 + row) * p.num_heads + u.head) * 128);
-      if (p.o_align32) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          st_global_v8(dst + q * 32, w0[q]);
-          st_global_v8(dst + 128 + q * 32, w1[q]);
-        }
-      } else {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          reinterpret_cast<uint4*>(dst + q * 32)[0] = make_uint4(w0[q][0], w0[q][1], w0[q][2], w0[q][3]);
-          reinterpret_cast<uint4*>(dst + q * 32)[1] = make_uint4(w0[q][4], w0[q][5], w0[q][6], w0[q][7]);
-          reinterpret_cast<uint4*>(dst + 128 + q * 32)[0] = make_uint4(w1[q][0], w1[q][1], w1[q][2], w1[q][3]);
-          reinterpret_cast<uint4*>(dst + 128 + q * 32)[1] = make_uint4(w1[q][4], w1[q][5], w1[q][6], w1[q][7]);
+    if constexpr (!kMerge) {
+      const float inv = empty ? 0.f : 1.f / l_row;
+      uint32_t w0[4][8], w1[4][8];
+      load_scaled_half(lane_addr + TM_O, inv, w0);
+      load_scaled_half(lane_addr + TM_O + 64, inv, w1);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(OFR));
+      // (The row address is formed twice on purpose: holding it across the stores
+      // costs registers this warpgroup does not have.)
+      if (live)
+        store_row(reinterpret_cast<char*>(p.o + ((size_t)(u.q_row0 + row) * p.num_heads + u.head) * 128),
+                  p.o_align32, w0, w1);
+      if (p.lse && live) {
+        float lg;
+        asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(l_row));
+        p.lse[(size_t)(u.q_row0 + row) * p.num_heads + u.head] = empty ? NEG_INF : (m_row + lg) * 0.6931471805599453f;
+      }
+    } else {
+      // Merge with the entry state (O_a, la): O = a * O_a + b * acc, LSE = lse2_out
+      // (log2 units), the weights taken in base 2 from both LSEs.
+      float a = 0.f, b = 0.f, lse2_out = NEG_INF;
+      if (live) {
+        float lg;
+        asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(l_row));
+        const float lse2_new = empty ? NEG_INF : m_row + lg;
+        const float lse2_old = p.lse[(size_t)(u.q_row0 + row) * p.num_heads + u.head] * 1.4426950408889634f;
+        const float mx = fmaxf(lse2_old, lse2_new);   // -inf only if both sides are empty
+        if (mx != NEG_INF) {
+          const float w_old = ex2_approx(lse2_old - mx), w_new = ex2_approx(lse2_new - mx);
+          const float sum = w_old + w_new, inv_sum = 1.f / sum;
+          float ls;
+          asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(ls) : "f"(sum));
+          a = w_old * inv_sum;
+          b = empty ? 0.f : w_new * inv_sum / l_row;
+          lse2_out = mx + ls;
         }
       }
-    }
-    if (p.lse && row < u.q_rows) {
-      float lg;
-      asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(lg) : "f"(l_row));
-      p.lse[(size_t)(u.q_row0 + row) * p.num_heads + u.head] = empty ? NEG_INF : (m_row + lg) * 0.6931471805599453f;
+      uint32_t w0[4][8], w1[4][8];
+      load_scaled_half(lane_addr + TM_O, b, w0);
+      load_scaled_half(lane_addr + TM_O + 64, b, w1);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(OFR));
+      if (live) {
+        // A side with LSE = -inf gets weight 0 and its O is never read.  One half at a
+        // time, merged then stored (the barrier keeps the second half's loads below the
+        // first half's stores, which bounds the registers in use).
+        char* dst = reinterpret_cast<char*>(p.o + ((size_t)(u.q_row0 + row) * p.num_heads + u.head) * 128);
+        if (a != 0.f) merge_old(dst, a, w0);
+        store_half(dst, p.o_align32, w0);
+        asm volatile("" ::: "memory");
+        if (a != 0.f) merge_old(dst + 128, a, w1);
+        store_half(dst + 128, p.o_align32, w1);
+      }
+      if (live)
+        p.lse[(size_t)(u.q_row0 + row) * p.num_heads + u.head] =
+            lse2_out == NEG_INF ? NEG_INF : lse2_out * 0.6931471805599453f;
     }
     g += n;
     ++k;
   }
 }
 
+// kMerge: o/lse hold a partial state that the epilogue merges this attention into.
+template <bool kMerge>
 __global__ void __launch_bounds__(NTHREADS, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -508,7 +602,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
   float* xchg = reinterpret_cast<float*>(smem + OFF_XCHG);
   if (warp < 4) {
-    setmaxnreg_dec<CTRL_REGS>();
+    setmaxnreg_dec<RegSplit<kMerge>::ctrl>();
     if (lane == 0) {
       if (warp == 0) run_producer_qk(c, p, &tm_q, &tm_k, ubeg, uend);
       else if (warp == 1) run_mma_qk(c, p, tmem, ubeg, uend);
@@ -516,11 +610,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       else run_mma_pv(c, p, tmem, ubeg, uend);
     }
   } else if (warp < 12) {
-    setmaxnreg_inc<SOFTMAX_REGS>();
-    run_softmax(c, p, tmem, xchg, ubeg, uend);
+    setmaxnreg_inc<RegSplit<kMerge>::softmax>();
+    run_softmax<kMerge>(c, p, tmem, xchg, ubeg, uend);
   } else {
-    setmaxnreg_dec<EPI_REGS>();
-    run_epilogue(c, p, tmem, xchg, ubeg, uend);
+    setmaxnreg_dec<RegSplit<kMerge>::epi>();
+    run_epilogue<kMerge>(c, p, tmem, xchg, ubeg, uend);
   }
   tc_fence_before();
   __syncthreads();
@@ -535,25 +629,32 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
 int prefill_smem_bytes() { return SMEM_BYTES; }
 
-cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const PrefillParams& p, int num_ctas, cudaStream_t stream) {
+template <bool kMerge>
+static cudaError_t launch_prefill_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                    const PrefillParams& p, int num_ctas, cudaStream_t stream) {
   static int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    e = cudaFuncSetAttribute(prefill_kernel<kMerge>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     // The warpgroups' setmaxnreg split assumes every thread starts with LAUNCH_REGS
     // registers; with fewer, the softmax warpgroups' increase could never be granted.
     cudaFuncAttributes attr;
-    e = cudaFuncGetAttributes(&attr, prefill_kernel);
+    e = cudaFuncGetAttributes(&attr, prefill_kernel<kMerge>);
     if (e != cudaSuccess) return e;
     if (attr.numRegs != LAUNCH_REGS) return cudaErrorInvalidConfiguration;
     configured_device = dev;
   }
-  prefill_kernel<<<num_ctas, NTHREADS, SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  prefill_kernel<kMerge><<<num_ctas, NTHREADS, SMEM_BYTES, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
+}
+
+cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const PrefillParams& p, int num_ctas, cudaStream_t stream) {
+  return p.merge ? launch_prefill_t<true>(tq, tk, tv, p, num_ctas, stream)
+                 : launch_prefill_t<false>(tq, tk, tv, p, num_ctas, stream);
 }
 
 }  // namespace mla

@@ -16,7 +16,9 @@ struct PrefillParams {
   const int32_t* cta_offsets; // [grid + 1]
   int* status;                // device status word (MLA_DEVSTAT_* bits)
   __nv_bfloat16* o;           // [total_q, H, 128]
-  float* lse;                 // [total_q, H] or null
+  float* lse;                 // [total_q, H] or null (never null when merge is set)
+  int merge;                  // o/lse hold a partial state on entry: write its LSE merge
+                              // with this attention instead of the attention alone
   int num_heads;
   int o_align32;              // o is 32-byte aligned: the epilogue uses 32-byte stores
   int causal;

@@ -124,9 +124,10 @@ int mla_prefill_plan(mla_plan_t* out, const int32_t* qo_indptr, const int32_t* k
   return MLA_OK;
 }
 
-int mla_prefill_run(mla_plan_t p, const void* q, const void* k, const void* v, void* o, float* lse,
-                    void* stream) {
+static int prefill_run_impl(mla_plan_t p, const void* q, const void* k, const void* v, void* o, float* lse,
+                            int merge, void* stream) {
   if (!p) return MLA_ERR_INVALID_ARG;
+  if (merge && !lse) return MLA_ERR_INVALID_ARG;
   if (p->plan.units.empty()) return MLA_OK;   // no query rows
   if (!q || !o || !aligned16(q) || !aligned16(o) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
     return MLA_ERR_INVALID_ARG;
@@ -163,6 +164,7 @@ int mla_prefill_run(mla_plan_t p, const void* q, const void* k, const void* v, v
   prm.o = static_cast<__nv_bfloat16*>(o);
   prm.o_align32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
   prm.lse = lse;
+  prm.merge = merge;
   prm.num_heads = p->num_heads;
   prm.causal = p->causal;
   prm.window_left = p->window_left;
@@ -173,6 +175,16 @@ int mla_prefill_run(mla_plan_t p, const void* q, const void* k, const void* v, v
   prm.x_to_cap = prm.has_cap ? p->sm_scale / p->soft_cap : 0.f;
   return launch_prefill(tq, tk, tv, prm, p->num_ctas, as_stream(stream)) == cudaSuccess ? MLA_OK
                                                                                      : MLA_ERR_CUDA;
+}
+
+int mla_prefill_run(mla_plan_t p, const void* q, const void* k, const void* v, void* o, float* lse,
+                    void* stream) {
+  return prefill_run_impl(p, q, k, v, o, lse, 0, stream);
+}
+
+int mla_prefill_run_merge(mla_plan_t p, const void* q, const void* k, const void* v, void* o, float* lse,
+                          void* stream) {
+  return prefill_run_impl(p, q, k, v, o, lse, 1, stream);
 }
 
 int mla_prefill_status(mla_plan_t p) {

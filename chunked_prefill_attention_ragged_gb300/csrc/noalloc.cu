@@ -117,6 +117,7 @@ extern "C" MLA_API int mla_prefill_run_noalloc(const int32_t* qo_indptr, const i
     return MLA_ERR_CUDA;
 
   PrefillParams prm;
+  prm.merge = 0;
   prm.units = d_units;
   prm.cta_offsets = d_offsets;
   prm.status = d_status;

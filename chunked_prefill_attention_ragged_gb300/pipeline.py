@@ -10,8 +10,10 @@ prefix lives in the paged cache as 512 latent + 64 rope per token and is
 decompressed before attention.
 
 Per run: new-token attention -> one gather of every chunk's latent rows ->
-for every chunk: up-projection -> non-causal attention -> in-place LSE merge
-into the running (O, LSE).  Chunking bounds the decompressed K/V (per chunk
+for every chunk: up-projection -> non-causal attention merged into the
+running (O, LSE) by the attention kernel's epilogue (mla_prefill_run_merge;
+with fuse_merge=False, the attention writes its own O/LSE and
+mla_merge_state merges them, the same result up to rounding).  Chunking bounds the decompressed K/V (per chunk
 tokens x heads x 640 bytes); the compressed rows are small (1152 bytes per
 token), so all chunks are gathered by one launch, which keeps that copy large
 enough to run near HBM bandwidth.  Every step is a kernel of
@@ -33,7 +35,7 @@ class ChunkedPrefill:
     """
 
     def __init__(self, qo_indptr, cu_seq_lens, chunk_starts, num_heads: int, *, sm_scale: float,
-                 logits_soft_cap: float = 0.0, device="cuda", stream=None):
+                 logits_soft_cap: float = 0.0, device="cuda", stream=None, fuse_merge: bool = True):
         import torch
         self.num_heads = num_heads
         qo = np.asarray(qo_indptr, dtype=np.int32)
@@ -72,8 +74,12 @@ class ChunkedPrefill:
         self.latent = torch.empty((max(self.total_prefix, 1), 576), dtype=bf, device=device)
         self.k_c = torch.empty((max(t_max, 1), h, 192), dtype=bf, device=device)
         self.v_c = torch.empty((max(t_max, 1), h, 128), dtype=bf, device=device)
-        self.o_c = torch.empty((max(self.total_q, 1), h, 128), dtype=bf, device=device)
-        self.lse_c = torch.empty((max(self.total_q, 1), h), dtype=torch.float32, device=device)
+        self.fuse_merge = bool(fuse_merge)
+        if self.fuse_merge:
+            self.o_c = self.lse_c = None
+        else:
+            self.o_c = torch.empty((max(self.total_q, 1), h, 128), dtype=bf, device=device)
+            self.lse_c = torch.empty((max(self.total_q, 1), h), dtype=torch.float32, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
 
     def chunk_table(self, block_table):
@@ -110,9 +116,12 @@ class ChunkedPrefill:
             lat = self.latent[self.row0[c]:self.row0[c] + t]
             kc, vc = self.k_c[:t], self.v_c[:t]
             mla_up_proj(lat, w_kvb, self.num_heads, kc, vc, self.status, stream)
-            oc, lc = self.o_c[:self.total_q], self.lse_c[:self.total_q]
-            plan.run(q, kc, vc, oc, lc, True, stream)
-            mla_merge_state(o, lse, oc, lc, o, lse, stream)
+            if self.fuse_merge:
+                plan.run_merge(q, kc, vc, o, lse, stream)
+            else:
+                oc, lc = self.o_c[:self.total_q], self.lse_c[:self.total_q]
+                plan.run(q, kc, vc, oc, lc, True, stream)
+                mla_merge_state(o, lse, oc, lc, o, lse, stream)
         return o, lse
 
     def check_status(self):

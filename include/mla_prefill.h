@@ -115,6 +115,26 @@ MLA_API int mla_prefill_run(mla_plan_t plan, const void* q, const void* k, const
                     float* lse, void* stream);
 
 /*
+ * Run a planned problem and merge its result into a partial state, in one
+ * kernel: the chunked-prefix step of [vLLM-FI] (run_prefill_context_chunk
+ * returns LSE so that chunk results merge with the new tokens' result).
+ * Same arguments, layout and checks as mla_prefill_run, except:
+ *   o   : bf16 [qo_indptr[batch], num_heads, 128], read and written: on entry a
+ *         partial attention output over other keys, on return the merge
+ *   lse : fp32 [qo_indptr[batch], num_heads], natural log, read and written;
+ *         required (NULL gives MLA_ERR_INVALID_ARG)
+ * With (O_a, la) the entry state and (O_b, lb) this attention, every row gets
+ * the mla_merge_state result: O = (e^{la-m} O_a + e^{lb-m} O_b) / (e^{la-m} +
+ * e^{lb-m}), LSE = m + ln(...), m = max(la, lb).  A side with LSE = -inf
+ * contributes nothing (its O is not read): rows that see no key here keep
+ * their entry state, and rows with LSE = -inf on both sides get O = 0.  O_b is
+ * rounded to bf16 before the merge, as it would be if it were written out and
+ * merged by mla_merge_state.
+ */
+MLA_API int mla_prefill_run_merge(mla_plan_t plan, const void* q, const void* k, const void* v, void* o,
+                                  float* lse, void* stream);
+
+/*
  * Read and clear the plan's device status word (a blocking device-to-host
  * copy; call after the run's stream has completed).  Returns MLA_OK,
  * MLA_ERR_DEVICE_TIMEOUT or MLA_ERR_CUDA.
