@@ -21,7 +21,10 @@
 //               end of a unit they only publish each row's sum and max and go on.
 //   warps 12-15 epilogue: read O from TMEM once the unit's last P V is done, release
 //               it for the next unit's first P V, then normalise, write O (bf16) and
-//               the natural-log LSE (fp32), off the softmax warps' critical path.
+//               the natural-log LSE (fp32), off the softmax warps' critical path.  In
+//               the merging instance (kMerge) they instead merge the result into the
+//               partial (O, LSE) state already in memory: the chunk step of chunked
+//               prefill, where run_prefill_context_chunk's LSE serves that merge.
 // TMEM: S buffers 0-2 (128 columns each; P overwrites the front of its S as bf16), O.
 // Every pipeline wait is bounded: on time-out the CTA records MLA_DEVSTAT_TIMEOUT,
 // drains its own copies and MMAs, frees TMEM and returns.
