@@ -61,6 +61,7 @@ def test_plan_rejects_bad_arguments_without_touching_the_device():
 def test_entry_points_reject_null_and_misaligned():
     lib = mla.library()
     assert lib.mla_prefill_run(None, None, None, None, None, None, None) == -1
+    assert lib.mla_prefill_run_merge(None, None, None, None, None, None, None) == -1
     assert lib.mla_prefill_status(None) == -1
     assert lib.mla_plan_destroy(None) == 0
     assert lib.mla_merge_state(None, None, None, None, None, None, 4, 2, 128, None) == -1

@@ -94,3 +94,18 @@ def test_run_merge_matches_oracle_merge(causal):
     o_ref, lse_ref = merge_state(np.where(dead[..., None], 0, o_a).astype(np.uint16), lse_a, o_b, lse_b)
     assert not bool(torch.isnan(o).any())
     check_attention(f64_of_bf16(o), lse.double().cpu().numpy(), o_ref, lse_ref, f"run_merge causal={causal}")
+
+
+def test_run_merge_requires_lse():
+    """The merge entry point reads the entry LSE: a NULL lse is rejected on the host."""
+    import ctypes
+    import chunked_prefill_attention_ragged_gb300 as mla
+    b = wl.random_ragged(59, [40], [90], 2, causal=False)
+    plan = mla.mla_prefill_plan(b.qo_indptr, b.kv_indptr, 2, causal=False, sm_scale=b.sm_scale)
+    q, k, v = to_dev_bf16(b.q), to_dev_bf16(b.k), to_dev_bf16(b.v)
+    o = torch.zeros(40, 2, 128, dtype=torch.bfloat16, device="cuda")
+    vp = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    rc = mla.library().mla_prefill_run_merge(plan.handle, vp(q), vp(k), vp(v), vp(o), None, None)
+    assert rc == -1
+    with pytest.raises(ValueError):
+        plan.run_merge(q, k, v, o, None)
