@@ -241,6 +241,19 @@ def random_chunked_prefix(seed: int, new_lens, prefix_lens, num_heads: int, *,
     return ChunkedPrefixBatch(new, prefix_lens, cache, table, w, block_size, chunk_tokens)
 
 
+def random_fp8_cache(rng: np.random.Generator, num_blocks: int, block_size: int,
+                     scale_exp=(119, 130)) -> np.ndarray:
+    """A paged cache of fp8 latent entries, uint8 [num_blocks, block_size, 648]: 512 random
+    float8 e4m3 codes (NaN codes 0x7F/0xFF excluded), 64 bf16 N(0,1) rope values (128 bytes)
+    and 8 scale exponent bytes drawn uniformly from ``scale_exp`` (inclusive)."""
+    n = num_blocks * block_size
+    codes = rng.integers(0, 254, size=(n, 512), dtype=np.uint16)
+    codes = np.where(codes >= 0x7F, codes + 1, codes).astype(np.uint8)      # skip 0x7F; 0xFF is never drawn
+    rope = _normal_bf16(rng, (n, 64)).view(np.uint8).reshape(n, 128)
+    scales = rng.integers(scale_exp[0], scale_exp[1] + 1, size=(n, 8)).astype(np.uint8)
+    return np.concatenate([codes, rope, scales], axis=1).reshape(num_blocks, block_size, 648)
+
+
 def make_chunked_prefix() -> ChunkedPrefixBatch:
     """Workload 2: 4 requests x (2048 new + 8192 cached), 128 heads, 4096-token chunks."""
     rng = np.random.default_rng(1002)

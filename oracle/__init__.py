@@ -20,6 +20,9 @@ computes, written from the pages' definitions:
     (sglang issue #3849: 512 latent + 64 rope cached, attention runs as MHA
     with 192-dim Q/K and 128-dim V);
   * the LSE merge of two partial attention states;
+  * the fp8 latent cache entry (fp8 latent with power-of-two scales per 64
+    values, bf16 rope; vLLM ``sparse_mla.py``'s ``fp8_ds_mla`` layout) and its
+    dequantizing gather;
   * the unchunked attention that chunked prefill must reproduce.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
@@ -33,7 +36,8 @@ closed forms and invariants.  Parity pins: attention (brute force, closed
 forms, invariants), gather (hand fixture + brute force), cache write (hand
 fixture, round trip through the gather, padding slots), up-projection
 (hand fixture + triple loop), merge (closed forms + split/merge identity),
-chunked pipeline (split/merge identity).  No function is "parity unpinned".
+chunked pipeline (split/merge identity), fp8 entries (hand-decoded codes, every
+e4m3 code against the library's float8 type, exact products).  No function is "parity unpinned".
 """
 from .bf16 import bf16_bits_to_f64, round_f64_to_bf16
 from .attention import allowed_mask, attend_request, ragged_attention
@@ -42,9 +46,12 @@ from .cache_write import cache_write
 from .up_proj import up_project
 from .merge import merge_state
 from .chunked import chunked_prefill_attention
+from .fp8_cache import (dequant_fp8_entries, e4m3_to_f64, f64_to_bf16_bits, gather_latent_fp8,
+                        ue8m0_to_f64)
 
 __all__ = [
     "bf16_bits_to_f64", "round_f64_to_bf16", "allowed_mask", "attend_request",
     "ragged_attention", "gather_latent", "slot_of", "cache_write", "up_project", "merge_state",
-    "chunked_prefill_attention",
+    "chunked_prefill_attention", "dequant_fp8_entries", "e4m3_to_f64", "f64_to_bf16_bits",
+    "gather_latent_fp8", "ue8m0_to_f64",
 ]
