@@ -8,11 +8,13 @@ names, plus the seeded workload generators.  Importing it loads nothing; the fir
 (if needed) and loads the library, and raises if that fails.
 """
 from ._binding import (EXPORTED, MlaError, PrefillPlan, error_string, library, library_path,
-                       mla_cache_write, mla_gather_latent, mla_merge_state, mla_plan_destroy, mla_plan_units_host,
-                       mla_prefill_plan, mla_prefill_run, mla_prefill_run_merge, mla_prefill_status, mla_up_proj)
+                       mla_cache_write, mla_gather_latent, mla_gather_latent_fp8, mla_merge_state, mla_plan_destroy, mla_plan_units_host,
+                       mla_prefill_plan, mla_prefill_run, mla_prefill_run_merge, mla_prefill_status, mla_up_proj,
+                       mla_up_proj_paged)
 
 __all__ = [
     "EXPORTED", "MlaError", "PrefillPlan", "error_string", "library", "library_path",
-    "mla_cache_write", "mla_gather_latent", "mla_merge_state", "mla_plan_destroy", "mla_plan_units_host",
+    "mla_cache_write", "mla_gather_latent", "mla_gather_latent_fp8", "mla_merge_state", "mla_plan_destroy", "mla_plan_units_host",
     "mla_prefill_plan", "mla_prefill_run", "mla_prefill_run_merge", "mla_prefill_status", "mla_up_proj",
+    "mla_up_proj_paged",
 ]

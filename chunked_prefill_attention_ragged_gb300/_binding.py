@@ -37,8 +37,12 @@ _SIGNATURES = {
                                      _i64p]),
     "mla_gather_latent": (_c_int, [_c_vp, _c_i64, _c_int, _c_int, _c_vp, _c_int, _c_vp, _c_vp, _c_int, _c_i64,
                                    _c_vp, _c_vp, _c_vp]),
+    "mla_gather_latent_fp8": (_c_int, [_c_vp, _c_i64, _c_int, _c_int, _c_vp, _c_int, _c_vp, _c_vp, _c_int, _c_i64,
+                                       _c_vp, _c_vp, _c_vp]),
     "mla_cache_write": (_c_int, [_c_vp, _c_i64, _c_int, _c_int, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp]),
     "mla_up_proj": (_c_int, [_c_vp, _c_vp, _c_i64, _c_int, _c_vp, _c_vp, _c_vp, _c_vp]),
+    "mla_up_proj_paged": (_c_int, [_c_vp, _c_i64, _c_int, _c_int, _c_vp, _c_int, _c_vp, _c_vp, _c_int, _c_i64,
+                                   _c_vp, _c_int, _c_vp, _c_vp, _c_vp, _c_vp]),
     "mla_merge_state": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_int, _c_int, _c_vp]),
     "mla_prefill_run_noalloc": (_c_int, [_i32p, _i32p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_f, _c_int, _c_f,
                                          _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
@@ -258,6 +262,30 @@ def mla_gather_latent(cache, block_table, cu_seq_lens, chunk_starts, total_token
     return out
 
 
+def mla_gather_latent_fp8(cache, block_table, cu_seq_lens, chunk_starts, total_tokens: int, out=None, status=None,
+                          stream=None):
+    """One prefix chunk out of an fp8 paged cache (uint8 [NB, BS, 648]), dequantized to
+    bf16 [total_tokens, 576]."""
+    import torch
+    nb, bs, e = cache.shape
+    t = int(total_tokens)
+    if out is None:
+        out = torch.empty((t, 576), dtype=torch.bfloat16, device=cache.device)
+    if tuple(out.shape) != (t, 576):
+        raise ValueError(f"out must be [{t}, 576]")
+    batch = block_table.shape[0]
+    if tuple(cu_seq_lens.shape) != (batch + 1,) or tuple(chunk_starts.shape) != (batch,):
+        raise ValueError("cu_seq_lens must be [B+1] and chunk_starts [B] for a block table of B rows")
+    i32 = torch.int32
+    _check(library().mla_gather_latent_fp8(_dev(cache, torch.uint8, "cache"), nb, bs, e,
+                                           _dev(block_table, i32, "block_table"), block_table.shape[1],
+                                           _dev(cu_seq_lens, i32, "cu_seq_lens"),
+                                           _dev(chunk_starts, i32, "chunk_starts"), batch, t,
+                                           _dev(out, torch.bfloat16, "out"), _dev(status, i32, "status"),
+                                           _stream(stream)), "mla_gather_latent_fp8")
+    return out
+
+
 def mla_cache_write(cache, latent, slot_mapping, status=None, stream=None):
     """Store latent [T, E] rows into the paged cache [NB, BS, E] at slot_mapping [T] (int64,
     device; negative = padding token).  Returns the cache (written in place)."""
@@ -290,10 +318,45 @@ def mla_up_proj(latent, w_kvb, num_heads: int, k_out=None, v_out=None, status=No
     return k_out, v_out
 
 
+def mla_up_proj_paged(cache, block_table, cu_seq_lens, chunk_starts, total_tokens: int, w_kvb, num_heads: int,
+                      k_out=None, v_out=None, status=None, stream=None):
+    """One prefix chunk decompressed straight from the paged cache [NB, BS, 576]:
+    K [T, H, 192], V [T, H, 128] (T = total_tokens), as gather + up-projection would give."""
+    import torch
+    nb, bs, e = cache.shape
+    t = int(total_tokens)
+    if e != 576 or tuple(w_kvb.shape) != (512, num_heads * 256):
+        raise ValueError("cache must be [NB, BS, 576] and w_kvb [512, H*256]")
+    batch = block_table.shape[0]
+    if tuple(cu_seq_lens.shape) != (batch + 1,) or tuple(chunk_starts.shape) != (batch,):
+        raise ValueError("cu_seq_lens must be [B+1] and chunk_starts [B] for a block table of B rows")
+    if k_out is None:
+        k_out = torch.empty((t, num_heads, 192), dtype=torch.bfloat16, device=cache.device)
+    if v_out is None:
+        v_out = torch.empty((t, num_heads, 128), dtype=torch.bfloat16, device=cache.device)
+    if tuple(k_out.shape) != (t, num_heads, 192) or tuple(v_out.shape) != (t, num_heads, 128):
+        raise ValueError("k_out/v_out shapes do not match total_tokens and num_heads")
+    bf, i32 = torch.bfloat16, torch.int32
+    _check(library().mla_up_proj_paged(_dev(cache, bf, "cache"), nb, bs, e, _dev(block_table, i32, "block_table"),
+                                       block_table.shape[1], _dev(cu_seq_lens, i32, "cu_seq_lens"),
+                                       _dev(chunk_starts, i32, "chunk_starts"), batch, t, _dev(w_kvb, bf, "w_kvb"),
+                                       num_heads, _dev(k_out, bf, "k_out"), _dev(v_out, bf, "v_out"),
+                                       _dev(status, i32, "status"), _stream(stream)), "mla_up_proj_paged")
+    return k_out, v_out
+
+
 def mla_merge_state(o_a, lse_a, o_b, lse_b, o_out=None, lse_out=None, stream=None):
     """Merge two partial states by LSE; o_out/lse_out may be o_a/lse_a (in place)."""
     import torch
     rows, h, d = o_a.shape
+    if tuple(o_b.shape) != (rows, h, d):
+        raise ValueError(f"o_b must be {(rows, h, d)} like o_a, got {tuple(o_b.shape)}")
+    if tuple(lse_a.shape) != (rows, h) or tuple(lse_b.shape) != (rows, h):
+        raise ValueError(f"lse_a and lse_b must be {(rows, h)}")
+    if o_out is not None and tuple(o_out.shape) != (rows, h, d):
+        raise ValueError(f"o_out must be {(rows, h, d)}")
+    if lse_out is not None and tuple(lse_out.shape) != (rows, h):
+        raise ValueError(f"lse_out must be {(rows, h)}")
     if o_out is None:
         o_out = torch.empty_like(o_a)
     if lse_out is None:
@@ -315,6 +378,18 @@ def mla_prefill_run_noalloc(qo_indptr, kv_indptr, num_heads: int, q, k, v, o, ls
     array inside the library, so overlapping calls must be serialised by the caller."""
     import torch
     qo, kv = _host_i32(qo_indptr), _host_i32(kv_indptr)
+    if qo.ndim != 1 or kv.shape != qo.shape or qo.size < 1:
+        raise ValueError("qo_indptr and kv_indptr must be 1-D of equal length batch+1")
+    total_q, total_kv = int(qo[-1]), int(kv[-1])
+    H = int(num_heads)
+    for t, shape, name in ((q, (total_q, H, 192), "q"), (k, (total_kv, H, 192), "k"), (v, (total_kv, H, 128), "v"),
+                           (o, (total_q, H, 128), "o")):
+        if t is None or tuple(t.shape) != shape:
+            raise ValueError(f"{name} must be {list(shape)}, got {None if t is None else tuple(t.shape)}")
+    if lse is not None and tuple(lse.shape) != (total_q, H):
+        raise ValueError(f"lse must be [{total_q}, {H}], got {tuple(lse.shape)}")
+    if status is not None and status.numel() < 1:
+        raise ValueError("status must hold at least one int32 word")
     bf = torch.bfloat16
     _check(library().mla_prefill_run_noalloc(
         _ptr(qo), _ptr(kv), qo.size - 1, num_heads, 192, 128, int(bool(causal)), float(sm_scale), int(window_left),

@@ -63,7 +63,8 @@ enum Bar {
   LR = 25,              // [unit parity] row sums and max of a unit published
   LFR = 27,             // [unit parity] the epilogue has read them
   OFR = 29,             // the epilogue has read O: the next unit's first P V may overwrite it
-  NBAR = 30
+  NEVER = 30,           // nothing arrives here: the time-out test mode waits on it
+  NBAR = 31
 };
 // Parity waits: a wait for phase f of a barrier is exact only while phase f - 1 has
 // completed and phase f + 1 cannot have.  O-done is split by tile parity so that the
@@ -94,17 +95,17 @@ constexpr uint32_t TM_O = 384;
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, 128, false, true);
 
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;    // 2 s
-constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;    // 0.2 s
+constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;    // 0.2 s: own copies and MMAs after an abort
 constexpr float RESCALE_THRESHOLD = 8.0f;             // log2 units
 
 struct Ctx {
   uint32_t sbase;
   volatile int* abort_flag;
   int* status;
+  uint64_t wait_limit_ns;
   __device__ uint32_t bar(int i) const { return sbase + OFF_BAR + 8 * i; }
   __device__ bool wait(int b, uint32_t parity) const {
-    return mbar_wait_bounded(bar(b), parity, abort_flag, status, MLA_DEVSTAT_TIMEOUT, WAIT_LIMIT_NS);
+    return mbar_wait_bounded(bar(b), parity, abort_flag, status, MLA_DEVSTAT_TIMEOUT, wait_limit_ns);
   }
   __device__ void drain(int b, uint32_t parity) const {
     int dummy = 0;
@@ -189,6 +190,9 @@ __device__ void run_mma_qk(const Ctx& c, const PrefillParams& p, uint32_t tmem, 
   bool ok = true;
   const uint64_t q_desc = sdesc_sw128(c.sbase + OFF_Q, 16, 1024);
   const uint64_t k_desc0 = sdesc_sw128(c.sbase + OFF_K, 16, 1024);
+  // Time-out test mode: phase 0 of NEVER never completes, so this wait gives up after
+  // the plan's limit and the whole CTA takes its abort path.
+  if (p.force_timeout) ok = c.wait(NEVER, 0);
   for (int ui = ubeg; ui < uend && ok; ++ui) {
     const Unit u = load_unit(p.units, ui);
     const int lo = u.kv_tiles & 0xFFFF, hi = (u.kv_tiles >> 16) & 0xFFFF;
@@ -298,9 +302,22 @@ __device__ void run_softmax(const Ctx& c, const PrefillParams& p, uint32_t tmem,
       tc_fence_after();
       float sv[64];
       tmem_ld64_sync(lane_addr + TM_S(b) + half * 64, reinterpret_cast<uint32_t*>(sv));
-      if (p.has_cap) {   // soft cap, already in log2 units afterwards
+      if (p.has_cap) {
+        // Soft cap c * tanh(sm_scale * x / c), in log2 units afterwards, from the identity
+        // tanh(y) = 1 - 2 / (e^(2y) + 1): one ex2 and one reciprocal on the SFU per logit
+        // (an overflowing e^(2y) gives 1, an underflowing one -1).
+        const float2 k2 = make_float2(p.cap_ex2_scale, p.cap_ex2_scale);
+        const float2 one = make_float2(1.f, 1.f);
+        const float2 m2c = make_float2(-2.f * p.cap_log2, -2.f * p.cap_log2);
+        const float2 c2 = make_float2(p.cap_log2, p.cap_log2);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) sv[i] = p.cap_log2 * tanhf(sv[i] * p.x_to_cap);
+        for (int i = 0; i < 32; ++i) {
+          const float2 a = fmul2(make_float2(sv[2 * i], sv[2 * i + 1]), k2);
+          const float2 d = fadd2(make_float2(ex2_approx(a.x), ex2_approx(a.y)), one);
+          const float2 r = ffma2(make_float2(rcp_approx(d.x), rcp_approx(d.y)), m2c, c2);
+          sv[2 * i] = r.x;
+          sv[2 * i + 1] = r.y;
+        }
       }
       const int kp0 = (lo + j) * BN + half * 64;
       const int c_hi = khi - kp0, c_lo = klo - kp0;
@@ -574,7 +591,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   int* abort_flag = reinterpret_cast<int*>(smem + OFF_MISC + 4);
-  Ctx c{smem_addr(smem), abort_flag, p.status};
+  Ctx c{smem_addr(smem), abort_flag, p.status, p.wait_limit_ns};
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBAR; ++i) mbar_init(c.bar(i), 1);
@@ -635,21 +652,19 @@ int prefill_smem_bytes() { return SMEM_BYTES; }
 template <bool kMerge>
 static cudaError_t launch_prefill_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                     const PrefillParams& p, int num_ctas, cudaStream_t stream) {
-  static int configured_device = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(prefill_kernel<kMerge>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
+  static PerDeviceOnce configured;
+  cudaError_t e = configured.run([] {
+    cudaError_t r = cudaFuncSetAttribute(prefill_kernel<kMerge>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SMEM_BYTES);
+    if (r != cudaSuccess) return r;
     // The warpgroups' setmaxnreg split assumes every thread starts with LAUNCH_REGS
     // registers; with fewer, the softmax warpgroups' increase could never be granted.
     cudaFuncAttributes attr;
-    e = cudaFuncGetAttributes(&attr, prefill_kernel<kMerge>);
-    if (e != cudaSuccess) return e;
-    if (attr.numRegs != LAUNCH_REGS) return cudaErrorInvalidConfiguration;
-    configured_device = dev;
-  }
+    r = cudaFuncGetAttributes(&attr, prefill_kernel<kMerge>);
+    if (r != cudaSuccess) return r;
+    return attr.numRegs == LAUNCH_REGS ? cudaSuccess : cudaErrorInvalidConfiguration;
+  });
+  if (e != cudaSuccess) return e;
   prefill_kernel<kMerge><<<num_ctas, NTHREADS, SMEM_BYTES, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }

@@ -61,8 +61,7 @@ cache_write_kernel(uint8_t* __restrict__ cache, int64_t num_slots, int row_bytes
     bulk_g2s(smem_addr(rows_smem), latent + row0 * row_bytes, bytes, bar_a);
   }
   // Every writing lane sees the batch land itself before reading it out.
-  int dummy = 0;
-  const bool landed = slot >= 0 && mbar_wait_bounded(bar_a, 0, &abort_flag, status ? status : &dummy,
+  const bool landed = slot >= 0 && mbar_wait_bounded(bar_a, 0, &abort_flag, status,
                                                      MLA_DEVSTAT_TIMEOUT, kWaitNs);
   if (landed) {
     bulk_s2g(cache + slot * row_bytes, smem_addr(rows_smem) + (uint32_t)lane * row_bytes, (uint32_t)row_bytes);
@@ -70,7 +69,7 @@ cache_write_kernel(uint8_t* __restrict__ cache, int64_t num_slots, int row_bytes
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
   // Lanes that wrote nothing must not leave the copy into shared memory outstanding.
-  if (lane == 0 && !(slot >= 0)) mbar_wait_bounded(bar_a, 0, &abort_flag, &dummy, MLA_DEVSTAT_TIMEOUT, kWaitNs);
+  if (lane == 0 && !(slot >= 0)) mbar_wait_bounded(bar_a, 0, &abort_flag, status, MLA_DEVSTAT_TIMEOUT, kWaitNs);
 }
 
 }  // namespace

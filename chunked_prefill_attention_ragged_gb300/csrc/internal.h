@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cstdint>
+#include <mutex>
 
 #include "../../include/mla_prefill.h"
 #include "planner.h"
@@ -27,7 +28,19 @@ struct PrefillParams {
   float scale_log2;           // sm_scale * log2(e)            (no soft cap)
   float cap_log2;             // logits_soft_cap * log2(e)     (soft cap)
   float x_to_cap;             // sm_scale / logits_soft_cap    (soft cap)
+  float cap_ex2_scale;        // 2 * log2(e) * sm_scale / logits_soft_cap: e^(2y) = 2^(x * this)
+  uint64_t wait_limit_ns;     // a pipeline wait gives up after this long (default 2 s)
+  int force_timeout;          // test mode: one wait that nothing satisfies (see below)
 };
+
+// Time-out test mode.  When the environment variable MLA_TEST_FORCE_TIMEOUT_NS holds a
+// value in 1 .. 2e9 at plan time, the plan's runs make one pipeline wait on a barrier
+// that nothing arrives on, with that value as every wait's limit: the wait gives up,
+// the kernel records MLA_DEVSTAT_TIMEOUT, drains its own copies and MMAs, frees TMEM
+// and returns.  Nothing faults or hangs; it lets tests drive the time-out path.
+// Returns 0 when the mode is off, else the limit in ns.
+uint64_t forced_timeout_ns();
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // the normal limit of a pipeline wait
 
 int prefill_smem_bytes();
 cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -45,6 +58,10 @@ cudaError_t launch_gather(const void* cache, int64_t num_blocks, int block_size,
                           const int32_t* cu_seq_lens, const int32_t* chunk_starts, int batch,
                           int64_t total_tokens, void* out, int32_t* status, cudaStream_t stream);
 
+cudaError_t launch_gather_fp8(const void* cache, int64_t num_blocks, int block_size, const int32_t* block_table,
+                              int max_blocks_per_req, const int32_t* cu_seq_lens, const int32_t* chunk_starts,
+                              int batch, int64_t total_tokens, void* out, int32_t* status, cudaStream_t stream);
+
 cudaError_t launch_cache_write(void* cache, int64_t num_slots, int entry_dim, const void* latent,
                                const int64_t* slot_mapping, int64_t num_tokens, int32_t* status,
                                cudaStream_t stream);
@@ -54,10 +71,40 @@ cudaError_t launch_up_proj(const CUtensorMap& ta, const CUtensorMap& tb, const v
                            int64_t num_tokens, int num_heads, void* k_out, void* v_out,
                            int32_t* status, cudaStream_t stream);
 
+cudaError_t launch_up_proj_paged(const CUtensorMap& ta, const CUtensorMap& tb, const void* cache, int64_t num_blocks,
+                                 int block_size, const int32_t* block_table, int max_blocks_per_req,
+                                 const int32_t* cu_seq_lens, const int32_t* chunk_starts, int batch,
+                                 int64_t total_tokens, int num_heads, void* k_out, void* v_out, int32_t* status,
+                                 cudaStream_t stream);
+
 cudaError_t launch_merge(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,
                          void* o_out, float* lse_out, int64_t rows, int num_heads, int head_dim,
                          cudaStream_t stream);
 
 int device_sm_count();
+
+// Runs a set-up step (kernel attributes, symbol lookups) once per device, from any
+// number of host threads: the first caller on a device runs it under a lock, later
+// callers see the recorded success.  A failed step is retried by the next call.
+class PerDeviceOnce {
+ public:
+  static constexpr int kMaxDevices = 64;
+  template <class F>
+  cudaError_t run(F&& setup) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mutex_);
+    if (done_[dev]) return cudaSuccess;
+    e = setup();
+    if (e == cudaSuccess) done_[dev] = true;
+    return e;
+  }
+
+ private:
+  std::mutex mutex_;
+  bool done_[kMaxDevices] = {};
+};
 
 }  // namespace mla

@@ -15,11 +15,21 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// Streaming 16-byte load.  The read-only (non-coherent) path is legal only for data no
+// thread of the kernel writes, so the first input takes the coherent path when the
+// outputs alias it (in-place merge).
+template <bool kReadOnly>
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
   uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
+  if constexpr (kReadOnly)
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+  else
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
+                 : "memory");
   return v;
 }
 
@@ -32,7 +42,9 @@ __device__ __forceinline__ uint32_t pack(float lo, float hi) {
   return r;
 }
 
-// log2(vec) lanes per (row, head); vec = head_dim / 8 <= 32.
+// log2(vec) lanes per (row, head); vec = head_dim / 8 <= 32.  kInPlace: o_out/lse_out may
+// alias o_a/lse_a, so those are read through coherent loads.
+template <bool kInPlace>
 __global__ void __launch_bounds__(kThreads)
 merge_kernel(const uint4* oa, const float* la, const uint4* ob, const float* lb, uint4* oo, float* lo,
              int64_t n_rh, int vec_shift) {
@@ -50,10 +62,10 @@ merge_kernel(const uint4* oa, const float* la, const uint4* ob, const float* lb,
     float a = 0.f, b = 0.f;
     uint4 va = make_uint4(0, 0, 0, 0), vb = va;
     if (live) {
-      a = __ldg(la + rh);
+      a = kInPlace ? la[rh] : __ldg(la + rh);
       b = __ldg(lb + rh);
-      va = ld_stream(oa + (rh << vec_shift) + e);
-      vb = ld_stream(ob + (rh << vec_shift) + e);
+      va = ld_stream<!kInPlace>(oa + (rh << vec_shift) + e);
+      vb = ld_stream<true>(ob + (rh << vec_shift) + e);
     }
     // Every lane of the group has read la/lb and its slice before any lane writes
     // (outputs may alias the first input).
@@ -96,9 +108,10 @@ cudaError_t launch_merge(const void* o_a, const float* lse_a, const void* o_b, c
   const int64_t want = (n_rh + groups_per_block - 1) / groups_per_block;
   const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 16;
   const int grid = (int)(want < cap ? want : cap);
-  merge_kernel<<<grid, kThreads, 0, stream>>>(static_cast<const uint4*>(o_a), lse_a,
-                                              static_cast<const uint4*>(o_b), lse_b,
-                                              static_cast<uint4*>(o_out), lse_out, n_rh, vec_shift);
+  const bool in_place = o_out == o_a || (lse_out != nullptr && lse_out == lse_a);
+  auto kernel = in_place ? merge_kernel<true> : merge_kernel<false>;
+  kernel<<<grid, kThreads, 0, stream>>>(static_cast<const uint4*>(o_a), lse_a, static_cast<const uint4*>(o_b),
+                                        lse_b, static_cast<uint4*>(o_out), lse_out, n_rh, vec_shift);
   return cudaGetLastError();
 }
 

@@ -13,10 +13,12 @@ struct mla_plan {
   int device = 0;
   int batch = 0, num_heads = 0, causal = 0, window_left = -1;
   float sm_scale = 0.f, soft_cap = 0.f;
+  uint64_t forced_timeout_ns = 0;   // test mode (see forced_timeout_ns())
   int64_t total_q = 0, total_kv = 0;
   PlanResult plan;
   int num_ctas = 0;
-  void* workspace = nullptr;     // units | cta offsets | status word
+  void* workspace = nullptr;     // units | cta offsets | status word (stream-ordered allocation)
+  cudaEvent_t last_use = nullptr;  // recorded after the upload and after every uncaptured run
   Unit* d_units = nullptr;
   int32_t* d_offsets = nullptr;
   int* d_status = nullptr;
@@ -27,6 +29,33 @@ namespace {
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// A non-blocking stream per device on which destroyed plans hand their workspace back,
+// in stream order after their last use, so that freeing never waits for the device.
+cudaStream_t release_stream(cudaError_t* err) {
+  static cudaStream_t streams[PerDeviceOnce::kMaxDevices] = {};
+  static PerDeviceOnce created;
+  *err = created.run([] {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    return cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking);
+  });
+  int dev = 0;
+  if (*err == cudaSuccess) *err = cudaGetDevice(&dev);
+  return *err == cudaSuccess ? streams[dev] : nullptr;
+}
+
+bool stream_capturing(cudaStream_t s) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &st) != cudaSuccess) return true;   // unknown: do not record
+  return st != cudaStreamCaptureStatusNone;
+}
+
+void free_plan_storage(mla_plan* p) {
+  if (p->last_use) cudaEventDestroy(p->last_use);
+  delete p;
+}
 
 }  // namespace
 
@@ -92,21 +121,27 @@ int mla_prefill_plan(mla_plan_t* out, const int32_t* qo_indptr, const int32_t* k
   p->window_left = window_left;
   p->sm_scale = sm_scale;
   p->soft_cap = logits_soft_cap > 0.f ? logits_soft_cap : 0.f;
+  p->forced_timeout_ns = forced_timeout_ns();
   p->total_q = qo_indptr[batch];
   p->total_kv = kv_indptr[batch];
   p->num_ctas = (int)p->plan.cta_offsets.size() - 1;
 
   const size_t units_bytes = round_up(std::max<size_t>(1, p->plan.units.size()) * sizeof(Unit), 256);
   const size_t offs_bytes = round_up(p->plan.cta_offsets.size() * sizeof(int32_t), 256);
-  if (cudaMalloc(&p->workspace, units_bytes + offs_bytes + 256) != cudaSuccess) {
-    delete p;
+  cudaStream_t s = as_stream(stream);
+  if (cudaEventCreateWithFlags(&p->last_use, cudaEventDisableTiming) != cudaSuccess) {
+    p->last_use = nullptr;
+    free_plan_storage(p);
+    return MLA_ERR_CUDA;
+  }
+  if (cudaMallocAsync(&p->workspace, units_bytes + offs_bytes + 256, s) != cudaSuccess) {
+    free_plan_storage(p);
     return MLA_ERR_CUDA;
   }
   char* ws = static_cast<char*>(p->workspace);
   p->d_units = reinterpret_cast<Unit*>(ws);
   p->d_offsets = reinterpret_cast<int32_t*>(ws + units_bytes);
   p->d_status = reinterpret_cast<int*>(ws + units_bytes + offs_bytes);
-  cudaStream_t s = as_stream(stream);
   cudaError_t e = cudaSuccess;
   if (!p->plan.units.empty())
     e = cudaMemcpyAsync(p->d_units, p->plan.units.data(), p->plan.units.size() * sizeof(Unit),
@@ -115,9 +150,11 @@ int mla_prefill_plan(mla_plan_t* out, const int32_t* qo_indptr, const int32_t* k
     e = cudaMemcpyAsync(p->d_offsets, p->plan.cta_offsets.data(), p->plan.cta_offsets.size() * sizeof(int32_t),
                         cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(p->d_status, 0, sizeof(int), s);
+  if (e == cudaSuccess) e = cudaEventRecord(p->last_use, s);
   if (e != cudaSuccess) {
-    cudaFree(p->workspace);
-    delete p;
+    cudaStreamSynchronize(s);
+    cudaFreeAsync(p->workspace, s);
+    free_plan_storage(p);
     return MLA_ERR_CUDA;
   }
   *out = p;
@@ -173,8 +210,15 @@ static int prefill_run_impl(mla_plan_t p, const void* q, const void* k, const vo
   prm.scale_log2 = p->sm_scale * LOG2E;
   prm.cap_log2 = prm.has_cap ? p->soft_cap * LOG2E : 0.f;
   prm.x_to_cap = prm.has_cap ? p->sm_scale / p->soft_cap : 0.f;
-  return launch_prefill(tq, tk, tv, prm, p->num_ctas, as_stream(stream)) == cudaSuccess ? MLA_OK
-                                                                                     : MLA_ERR_CUDA;
+  prm.cap_ex2_scale = 2.f * LOG2E * prm.x_to_cap;
+  prm.force_timeout = p->forced_timeout_ns != 0;
+  prm.wait_limit_ns = prm.force_timeout ? p->forced_timeout_ns : kWaitLimitNs;
+  const cudaStream_t s = as_stream(stream);
+  if (launch_prefill(tq, tk, tv, prm, p->num_ctas, s) != cudaSuccess) return MLA_ERR_CUDA;
+  // Remember the last use for mla_plan_destroy.  A run captured into a graph is not
+  // recorded: the plan must then outlive every launch of that graph.
+  if (!stream_capturing(s) && cudaEventRecord(p->last_use, s) != cudaSuccess) return MLA_ERR_CUDA;
+  return MLA_OK;
 }
 
 int mla_prefill_run(mla_plan_t p, const void* q, const void* k, const void* v, void* o, float* lse,
@@ -201,10 +245,21 @@ int mla_plan_destroy(mla_plan_t p) {
   if (!p) return MLA_OK;
   int rc = MLA_OK;
   if (p->workspace) {
-    if (cudaDeviceSynchronize() != cudaSuccess) rc = MLA_ERR_CUDA;
-    if (cudaFree(p->workspace) != cudaSuccess) rc = MLA_ERR_CUDA;
+    // Free in stream order after the plan's last recorded use, on a library stream of the
+    // plan's device: neither the host nor other streams wait.
+    int cur = 0;
+    const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
+    if (!have_cur || cur != p->device) {
+      if (cudaSetDevice(p->device) != cudaSuccess) rc = MLA_ERR_CUDA;
+    }
+    cudaError_t e = cudaSuccess;
+    cudaStream_t rs = rc == MLA_OK ? release_stream(&e) : nullptr;
+    if (rc == MLA_OK && e == cudaSuccess) e = cudaStreamWaitEvent(rs, p->last_use, 0);
+    if (rc == MLA_OK && e == cudaSuccess) e = cudaFreeAsync(p->workspace, rs);
+    if (e != cudaSuccess) rc = MLA_ERR_CUDA;
+    if (have_cur && cur != p->device) cudaSetDevice(cur);
   }
-  delete p;
+  free_plan_storage(p);
   return rc;
 }
 
@@ -237,6 +292,24 @@ int mla_gather_latent(const void* cache, int64_t num_blocks, int block_size, int
   return launch_gather(cache, num_blocks, block_size, entry_dim, block_table, max_blocks_per_req,
                        cu_seq_lens, chunk_starts, batch, total_tokens, out, status,
                        as_stream(stream)) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
+int mla_gather_latent_fp8(const void* cache, int64_t num_blocks, int block_size, int entry_bytes,
+                          const int32_t* block_table, int max_blocks_per_req, const int32_t* cu_seq_lens,
+                          const int32_t* chunk_starts, int batch, int64_t total_tokens, void* out, int32_t* status,
+                          void* stream) {
+  if (total_tokens < 0 || batch < 0 || num_blocks < 0 || block_size < 1 || max_blocks_per_req < 0)
+    return MLA_ERR_INVALID_ARG;
+  if (entry_bytes != 648) return MLA_ERR_UNSUPPORTED;
+  if (total_tokens == 0) return MLA_OK;
+  if (batch == 0) return MLA_ERR_SHAPE;
+  if (!cache || !block_table || !cu_seq_lens || !chunk_starts || !out || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(cache) & 7u) || (reinterpret_cast<uintptr_t>(status) & 3u))
+    return MLA_ERR_INVALID_ARG;
+  return launch_gather_fp8(cache, num_blocks, block_size, block_table, max_blocks_per_req, cu_seq_lens,
+                           chunk_starts, batch, total_tokens, out, status, as_stream(stream)) == cudaSuccess
              ? MLA_OK
              : MLA_ERR_CUDA;
 }
@@ -281,6 +354,44 @@ int mla_up_proj(const void* latent, const void* w_kvb, int64_t num_tokens, int n
   }
   return launch_up_proj(ta, tb, latent, num_tokens, num_heads, k_out, v_out, status, as_stream(stream)) ==
                  cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
+int mla_up_proj_paged(const void* cache, int64_t num_blocks, int block_size, int entry_dim,
+                      const int32_t* block_table, int max_blocks_per_req, const int32_t* cu_seq_lens,
+                      const int32_t* chunk_starts, int batch, int64_t total_tokens, const void* w_kvb, int num_heads,
+                      void* k_out, void* v_out, int32_t* status, void* stream) {
+  if (total_tokens < 0 || batch < 0 || num_blocks < 0 || block_size < 1 || max_blocks_per_req < 0 ||
+      num_heads < 1)
+    return MLA_ERR_INVALID_ARG;
+  if (entry_dim != 576) return MLA_ERR_UNSUPPORTED;
+  if (total_tokens == 0) return MLA_OK;
+  if (batch == 0) return MLA_ERR_SHAPE;
+  // Slots are TMA row coordinates (int32), and one past the last slot marks a missing row.
+  if (num_blocks * (int64_t)block_size >= 0x7fffffff || total_tokens > (int64_t)1 << 31) return MLA_ERR_UNSUPPORTED;
+  if (((total_tokens + 127) / 128) * (int64_t)num_heads > 0x7fffffff) return MLA_ERR_UNSUPPORTED;
+  if (!cache || !block_table || !cu_seq_lens || !chunk_starts || !w_kvb || !k_out || !v_out || !aligned16(cache) ||
+      !aligned16(w_kvb) || !aligned16(k_out) || !aligned16(v_out) || (reinterpret_cast<uintptr_t>(status) & 3u))
+    return MLA_ERR_INVALID_ARG;
+  CUtensorMap ta, tb;
+  {
+    const uint64_t slots = (uint64_t)num_blocks * (uint64_t)block_size;
+    const uint64_t dims[2] = {576, slots > 0 ? slots : 1};
+    const uint64_t strides[1] = {576 * 2};
+    const uint32_t box[2] = {64, 1};   // one row high: rows are fetched four at a time by gather4
+    if (make_tensor_map_bf16(&ta, cache, 2, dims, strides, box) != MLA_OK) return MLA_ERR_CUDA;
+  }
+  {
+    const uint64_t n = (uint64_t)num_heads * 256;
+    const uint64_t dims[2] = {n, 512};
+    const uint64_t strides[1] = {n * 2};
+    const uint32_t box[2] = {64, 64};
+    if (make_tensor_map_bf16(&tb, w_kvb, 2, dims, strides, box) != MLA_OK) return MLA_ERR_CUDA;
+  }
+  return launch_up_proj_paged(ta, tb, cache, num_blocks, block_size, block_table, max_blocks_per_req, cu_seq_lens,
+                              chunk_starts, batch, total_tokens, num_heads, k_out, v_out, status,
+                              as_stream(stream)) == cudaSuccess
              ? MLA_OK
              : MLA_ERR_CUDA;
 }

@@ -2,6 +2,7 @@
 // so the library needs no link-time dependency on libcuda.
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "internal.h"
@@ -40,6 +41,15 @@ int make_tensor_map_bf16(CUtensorMap* map, const void* base, int rank, const uin
                   gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
+}
+
+uint64_t forced_timeout_ns() {
+  const char* v = std::getenv("MLA_TEST_FORCE_TIMEOUT_NS");
+  if (!v || !*v) return 0;
+  char* end = nullptr;
+  const unsigned long long x = std::strtoull(v, &end, 10);
+  if (end == v || *end != '\0' || x < 1 || x > kWaitLimitNs) return 0;
+  return (uint64_t)x;
 }
 
 int device_sm_count() {

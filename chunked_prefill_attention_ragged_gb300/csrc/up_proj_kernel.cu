@@ -26,6 +26,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "paged.cuh"
 #include "ptx.cuh"
 #include "tmem_wide.cuh"
 
@@ -66,7 +67,7 @@ struct Ctx {
 };
 
 struct UpParams {
-  const __nv_bfloat16* latent;
+  const __nv_bfloat16* latent;   // [num_tokens, 576]; paged: the cache [num_slots, 576]
   __nv_bfloat16* k;
   __nv_bfloat16* v;
   int* status;
@@ -74,13 +75,31 @@ struct UpParams {
   int num_heads;
   int num_tiles;
   int out_align32;   // k and v 32-byte aligned: 32-byte stores
+  // paged form: token row t of the output is the cache row of the chunk's row t
+  RowMap rows;
+  int32_t oob_row;   // a row coordinate past the cache: the TMA fills it with zeros
 };
+
+// Cache slot of chunk row `row` for the paged form (all 32 lanes of the warp call; rows
+// past the chunk or with an unknown block give `p.oob_row` and, for rows inside the
+// chunk, flag MLA_DEVSTAT_BAD_INDEX).
+__device__ __forceinline__ int32_t paged_row(const UpParams& p, int64_t row, int32_t cu_l, int32_t st_l) {
+  const bool active = row < p.num_tokens;
+  int64_t slot = 0;
+  const bool ok = resolve_slot(p.rows, row, active, cu_l, st_l, &slot);
+  if (active && !ok && p.status) atomicOr(p.status, MLA_DEVSTAT_BAD_INDEX);
+  return ok ? (int32_t)slot : p.oob_row;
+}
 
 __device__ __forceinline__ void tile_range(int num_tiles, int& beg, int& end) {
   beg = (int)((int64_t)blockIdx.x * num_tiles / gridDim.x);
   end = (int)((int64_t)(blockIdx.x + 1) * num_tiles / gridDim.x);
 }
 
+// kPaged: the latent rows come straight out of the paged cache (tm_a maps the cache as
+// [num_slots, 576] rows; each token block's 128 rows are fetched four at a time by
+// tile::gather4 copies), so no gathered latent buffer is needed.
+template <bool kPaged>
 __global__ void __launch_bounds__(NTHREADS, 1)
 up_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                const UpParams p) {
@@ -111,34 +130,60 @@ up_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
   tile_range(p.num_tiles, tbeg, tend);
   const int H = p.num_heads;
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0) {
+    // Producer warp.  Lane 0 waits and issues W's slices; in the paged form every lane
+    // resolves four latent rows and issues their gather copies.
     int it = 0, a_loads = 0;
     bool ok = true;
     // W (32 MB for 128 heads) is read by every token block: keep it in L2 while the
     // much larger K/V output streams through.
     const uint64_t w_policy = l2_policy_evict_last();
+    int32_t cu_l = 0, st_l = 0;
+    if constexpr (kPaged) {
+      cu_l = p.rows.batch < 32 && lane <= p.rows.batch ? __ldg(p.rows.cu + lane) : 0x7fffffff;
+      st_l = p.rows.batch < 32 && lane < p.rows.batch ? __ldg(p.rows.starts + lane) : 0;
+    }
     for (int tile = tbeg; tile < tend && ok; ++tile) {
       const int m = tile / H, h = tile % H;
       if (tile == tbeg || h == 0) {   // new token block: reload the latent tile
-        if (a_loads > 0 && !c.wait(LE, (a_loads - 1) & 1)) { ok = false; break; }
-        mbar_arrive_expect_tx(c.bar(LF), A_BYTES);
-        for (int kb = 0; kb < KBLOCKS; ++kb)
-          tma_load_2d(c.sbase + OFF_A + kb * A_PANEL, &tm_a, c.bar(LF), kb * BK, m * BM);
+        int free = 1;
+        if (lane == 0 && a_loads > 0) free = c.wait(LE, (a_loads - 1) & 1);
+        if (!__shfl_sync(0xffffffffu, free, 0)) { ok = false; break; }
+        if (lane == 0) mbar_arrive_expect_tx(c.bar(LF), A_BYTES);
+        __syncwarp();
+        if constexpr (kPaged) {
+          // Lane l fetches token rows 4l .. 4l+3 of the block: one gather per 64-column panel.
+          int32_t r4[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) r4[j] = paged_row(p, (int64_t)m * BM + 4 * lane + j, cu_l, st_l);
+          for (int kb = 0; kb < KBLOCKS; ++kb)
+            tma_gather4(c.sbase + OFF_A + kb * A_PANEL + lane * 4 * 128, &tm_a, c.bar(LF), kb * BK, r4[0], r4[1],
+                        r4[2], r4[3]);
+        } else if (lane == 0) {
+          for (int kb = 0; kb < KBLOCKS; ++kb)
+            tma_load_2d(c.sbase + OFF_A + kb * A_PANEL, &tm_a, c.bar(LF), kb * BK, m * BM);
+        }
         ++a_loads;
       }
-      for (int kb = 0; kb < KBLOCKS; ++kb, ++it) {
-        const int s = it % NS;
-        const uint32_t use = it / NS;
-        if (use > 0 && !c.wait(EMPTY + s, (use - 1) & 1)) { ok = false; break; }
-        mbar_arrive_expect_tx(c.bar(FULL + s), B_BYTES);
-        for (int i = 0; i < 4; ++i)
-          tma_load_2d_hint(c.sbase + OFF_B + s * B_BYTES + i * B_PANEL, &tm_b, c.bar(FULL + s),
-                           h * BN + i * 64, kb * BK, w_policy);
+      int went = 1;
+      if (lane == 0) {
+        for (int kb = 0; kb < KBLOCKS; ++kb, ++it) {
+          const int s = it % NS;
+          const uint32_t use = it / NS;
+          if (use > 0 && !c.wait(EMPTY + s, (use - 1) & 1)) { went = 0; break; }
+          mbar_arrive_expect_tx(c.bar(FULL + s), B_BYTES);
+          for (int i = 0; i < 4; ++i)
+            tma_load_2d_hint(c.sbase + OFF_B + s * B_BYTES + i * B_PANEL, &tm_b, c.bar(FULL + s),
+                             h * BN + i * 64, kb * BK, w_policy);
+        }
       }
+      ok = __shfl_sync(0xffffffffu, went, 0) != 0;
     }
-    if (a_loads > 0) c.drain(LF, (a_loads - 1) & 1);
-    for (int s = 0; s < NS; ++s)
-      if (it > s) c.drain(FULL + s, ((it - 1 - s) / NS) & 1);
+    if (lane == 0) {
+      if (a_loads > 0) c.drain(LF, (a_loads - 1) & 1);
+      for (int s = 0; s < NS; ++s)
+        if (it > s) c.drain(FULL + s, ((it - 1 - s) / NS) & 1);
+    }
   } else if (warp == 1 && lane == 0) {
     int it = 0, acc = 0, a_loads = 0;
     bool ok = true;
@@ -179,15 +224,32 @@ up_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
     int acc = 0;
     uint4 rope[8];
     const uint64_t out_policy = l2_policy_evict_first();   // K/V are written once here
+    int32_t cu_l = 0, st_l = 0;
+    if constexpr (kPaged) {
+      cu_l = p.rows.batch < 32 && lane <= p.rows.batch ? __ldg(p.rows.cu + lane) : 0x7fffffff;
+      st_l = p.rows.batch < 32 && lane < p.rows.batch ? __ldg(p.rows.starts + lane) : 0;
+    }
     for (int tile = tbeg; tile < tend; ++tile, ++acc) {
       const int a = acc & 1;
       const int64_t t = (int64_t)(tile / H) * BM + row;
       const int h = tile % H;
       const bool live = t < p.num_tokens;
-      if ((tile == tbeg || h == 0) && live) {   // rope part of this token, the same for every head
-        const uint4* src = reinterpret_cast<const uint4*>(p.latent + t * 576 + 512);
+      if (tile == tbeg || h == 0) {   // rope part of this token, the same for every head
+        int64_t src_row = t;
+        bool have = live;
+        if constexpr (kPaged) {
+          int64_t slot = 0;
+          have = resolve_slot(p.rows, t, live, cu_l, st_l, &slot);   // warp-wide call
+          src_row = slot;
+        }
+        if (have) {
+          const uint4* src = reinterpret_cast<const uint4*>(p.latent + src_row * 576 + 512);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) rope[i] = __ldg(src + i);
+          for (int i = 0; i < 8; ++i) rope[i] = __ldg(src + i);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) rope[i] = make_uint4(0, 0, 0, 0);   // unknown block: zeros
+        }
       }
       if (!__all_sync(0xffffffffu, c.wait(AFULL + a, (acc >> 1) & 1))) break;
       tc_fence_after();
@@ -233,19 +295,25 @@ up_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
 
 int up_proj_smem_bytes() { return SMEM_BYTES; }
 
-cudaError_t launch_up_proj(const CUtensorMap& ta, const CUtensorMap& tb, const void* latent,
-                           int64_t num_tokens, int num_heads, void* k_out, void* v_out,
-                           int32_t* status, cudaStream_t stream) {
-  static int configured_device = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+template <bool kPaged>
+static cudaError_t launch_up_proj_t(const CUtensorMap& ta, const CUtensorMap& tb, UpParams& p, cudaStream_t stream) {
+  static PerDeviceOnce configured;
+  cudaError_t e = configured.run([] {
+    return cudaFuncSetAttribute(up_proj_kernel<kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  });
   if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(up_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
-  UpParams p;
+  const int64_t m_tiles = (p.num_tokens + BM - 1) / BM;
+  p.num_tiles = (int)(m_tiles * p.num_heads);
+  if (p.num_tiles == 0) return cudaSuccess;
+  const int sms = device_sm_count();
+  const int grid = p.num_tiles < sms ? p.num_tiles : (sms > 0 ? sms : 148);
+  up_proj_kernel<kPaged><<<grid, NTHREADS, SMEM_BYTES, stream>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+static UpParams up_params(const void* latent, int64_t num_tokens, int num_heads, void* k_out, void* v_out,
+                          int32_t* status) {
+  UpParams p{};
   p.latent = static_cast<const __nv_bfloat16*>(latent);
   p.k = static_cast<__nv_bfloat16*>(k_out);
   p.v = static_cast<__nv_bfloat16*>(v_out);
@@ -253,13 +321,25 @@ cudaError_t launch_up_proj(const CUtensorMap& ta, const CUtensorMap& tb, const v
   p.num_tokens = num_tokens;
   p.num_heads = num_heads;
   p.out_align32 = ((reinterpret_cast<uintptr_t>(k_out) | reinterpret_cast<uintptr_t>(v_out)) & 31u) == 0;
-  const int64_t m_tiles = (num_tokens + BM - 1) / BM;
-  p.num_tiles = (int)(m_tiles * num_heads);
-  if (p.num_tiles == 0) return cudaSuccess;
-  const int sms = device_sm_count();
-  const int grid = p.num_tiles < sms ? p.num_tiles : (sms > 0 ? sms : 148);
-  up_proj_kernel<<<grid, NTHREADS, SMEM_BYTES, stream>>>(ta, tb, p);
-  return cudaGetLastError();
+  return p;
+}
+
+cudaError_t launch_up_proj(const CUtensorMap& ta, const CUtensorMap& tb, const void* latent,
+                           int64_t num_tokens, int num_heads, void* k_out, void* v_out,
+                           int32_t* status, cudaStream_t stream) {
+  UpParams p = up_params(latent, num_tokens, num_heads, k_out, v_out, status);
+  return launch_up_proj_t<false>(ta, tb, p, stream);
+}
+
+cudaError_t launch_up_proj_paged(const CUtensorMap& ta, const CUtensorMap& tb, const void* cache, int64_t num_blocks,
+                                 int block_size, const int32_t* block_table, int max_blocks_per_req,
+                                 const int32_t* cu_seq_lens, const int32_t* chunk_starts, int batch,
+                                 int64_t total_tokens, int num_heads, void* k_out, void* v_out, int32_t* status,
+                                 cudaStream_t stream) {
+  UpParams p = up_params(cache, total_tokens, num_heads, k_out, v_out, status);
+  p.rows = RowMap{cu_seq_lens, chunk_starts, block_table, batch, max_blocks_per_req, block_size, num_blocks};
+  p.oob_row = (int32_t)(num_blocks * block_size);
+  return launch_up_proj_t<true>(ta, tb, p, stream);
 }
 
 }  // namespace mla

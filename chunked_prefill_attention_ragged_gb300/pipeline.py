@@ -9,14 +9,18 @@ chunk's LSE so the partial outputs can be merged.  sglang issue #3849: the
 prefix lives in the paged cache as 512 latent + 64 rope per token and is
 decompressed before attention.
 
-Per run: new-token attention -> one gather of every chunk's latent rows ->
-for every chunk: up-projection -> non-causal attention merged into the
-running (O, LSE) by the attention kernel's epilogue (mla_prefill_run_merge;
-with fuse_merge=False, the attention writes its own O/LSE and
-mla_merge_state merges them, the same result up to rounding).  Chunking bounds the decompressed K/V (per chunk
-tokens x heads x 640 bytes); the compressed rows are small (1152 bytes per
-token), so all chunks are gathered by one launch, which keeps that copy large
-enough to run near HBM bandwidth.  Every step is a kernel of
+Per run: new-token attention -> for every chunk: the chunk's K/V decompressed
+straight out of the paged cache (mla_up_proj_paged: gather and up-projection in
+one kernel, no gathered latent buffer) -> non-causal attention merged into the
+running (O, LSE) by the attention kernel's epilogue (mla_prefill_run_merge).
+Variants, the same result up to rounding: with paged_up_proj=False one gather
+of every chunk's latent rows (one launch, large enough to run near HBM
+bandwidth) feeds mla_up_proj; with fuse_merge=False the attention writes its
+own O/LSE and mla_merge_state merges them.  With cache_fp8=True the cache holds
+648-byte fp8 entries (vLLM sparse_mla.py's fp8_ds_mla layout, see
+mla_gather_latent_fp8): one dequantizing gather of every chunk feeds
+mla_up_proj.  Chunking bounds the decompressed
+K/V (per chunk tokens x heads x 640 bytes).  Every step is a kernel of
 libmla_prefill.so; this class only owns buffers and orders the calls on one
 stream.
 """
@@ -24,7 +28,8 @@ from __future__ import annotations
 
 import numpy as np
 
-from ._binding import (mla_gather_latent, mla_merge_state, mla_prefill_plan, mla_up_proj)
+from ._binding import (mla_gather_latent, mla_gather_latent_fp8, mla_merge_state, mla_prefill_plan, mla_up_proj,
+                       mla_up_proj_paged)
 
 
 class ChunkedPrefill:
@@ -35,7 +40,8 @@ class ChunkedPrefill:
     """
 
     def __init__(self, qo_indptr, cu_seq_lens, chunk_starts, num_heads: int, *, sm_scale: float,
-                 logits_soft_cap: float = 0.0, device="cuda", stream=None, fuse_merge: bool = True):
+                 logits_soft_cap: float = 0.0, device="cuda", stream=None, fuse_merge: bool = True,
+                 paged_up_proj: bool = True, cache_fp8: bool = False):
         import torch
         self.num_heads = num_heads
         qo = np.asarray(qo_indptr, dtype=np.int32)
@@ -71,7 +77,10 @@ class ChunkedPrefill:
         t_max = max(self.chunk_tokens, default=0)
         h = num_heads
         bf = torch.bfloat16
-        self.latent = torch.empty((max(self.total_prefix, 1), 576), dtype=bf, device=device)
+        self.cache_fp8 = bool(cache_fp8)
+        self.paged_up_proj = bool(paged_up_proj) and not self.cache_fp8
+        self.latent = None if self.paged_up_proj else torch.empty((max(self.total_prefix, 1), 576), dtype=bf,
+                                                                   device=device)
         self.k_c = torch.empty((max(t_max, 1), h, 192), dtype=bf, device=device)
         self.v_c = torch.empty((max(t_max, 1), h, 128), dtype=bf, device=device)
         self.fuse_merge = bool(fuse_merge)
@@ -100,22 +109,27 @@ class ChunkedPrefill:
 
     def gather_all(self, cache, block_table, stream=None):
         """Every chunk's latent rows, one launch: self.latent[row0[c]:row0[c+1]] is chunk c."""
+        import torch
+        if self.latent is None:
+            self.latent = torch.empty((max(self.total_prefix, 1), 576), dtype=torch.bfloat16, device=cache.device)
         if self.total_prefix:
-            mla_gather_latent(cache, self.chunk_table(block_table), self.cu_all_dev, self.starts_all_dev,
-                              self.total_prefix, self.latent[:self.total_prefix], self.status, stream)
+            gather = mla_gather_latent_fp8 if self.cache_fp8 else mla_gather_latent
+            gather(cache, self.chunk_table(block_table), self.cu_all_dev, self.starts_all_dev, self.total_prefix,
+                   self.latent[:self.total_prefix], self.status, stream)
         return self.latent
 
     def run(self, q, k, v, cache, block_table, w_kvb, o=None, lse=None, stream=None):
-        """q/k/v: new tokens; cache [NB, BS, 576]; block_table [B, M] int32 (device)."""
+        """q/k/v: new tokens; cache [NB, BS, 576] bf16 (or [NB, BS, 648] uint8 with cache_fp8);
+        block_table [B, M] int32 (device)."""
         o, lse = self.main.run(q, k, v, o, lse, True, stream)
-        self.gather_all(cache, block_table, stream)
+        if not self.paged_up_proj:
+            self.gather_all(cache, block_table, stream)
         for c, plan in enumerate(self.chunks):
             t = self.chunk_tokens[c]
             if t == 0:
                 continue
-            lat = self.latent[self.row0[c]:self.row0[c] + t]
             kc, vc = self.k_c[:t], self.v_c[:t]
-            mla_up_proj(lat, w_kvb, self.num_heads, kc, vc, self.status, stream)
+            self.decompress(c, cache, block_table, w_kvb, kc, vc, stream)
             if self.fuse_merge:
                 plan.run_merge(q, kc, vc, o, lse, stream)
             else:
@@ -123,6 +137,16 @@ class ChunkedPrefill:
                 plan.run(q, kc, vc, oc, lc, True, stream)
                 mla_merge_state(o, lse, oc, lc, o, lse, stream)
         return o, lse
+
+    def decompress(self, c, cache, block_table, w_kvb, kc, vc, stream=None):
+        """Chunk c's K [T, H, 192] and V [T, H, 128] into kc, vc."""
+        t = self.chunk_tokens[c]
+        if self.paged_up_proj:
+            mla_up_proj_paged(cache, block_table, self.cu_dev[c], self.starts_dev[c], t, w_kvb, self.num_heads, kc, vc,
+                              self.status, stream)
+        else:
+            lat = self.latent[self.row0[c]:self.row0[c] + t]
+            mla_up_proj(lat, w_kvb, self.num_heads, kc, vc, self.status, stream)
 
     def check_status(self):
         """Raise if any kernel of the pipeline reported a device-side problem."""

@@ -242,13 +242,23 @@ def random_chunked_prefix(seed: int, new_lens, prefix_lens, num_heads: int, *,
 
 
 def random_fp8_cache(rng: np.random.Generator, num_blocks: int, block_size: int,
-                     scale_exp=(119, 130)) -> np.ndarray:
+                     scale_exp=(119, 130), code_exp=None) -> np.ndarray:
     """A paged cache of fp8 latent entries, uint8 [num_blocks, block_size, 648]: 512 random
     float8 e4m3 codes (NaN codes 0x7F/0xFF excluded), 64 bf16 N(0,1) rope values (128 bytes)
-    and 8 scale exponent bytes drawn uniformly from ``scale_exp`` (inclusive)."""
+    and 8 scale exponent bytes drawn uniformly from ``scale_exp`` (inclusive).
+
+    ``code_exp=(lo, hi)`` restricts the codes' 4-bit exponent field to lo..hi (random sign
+    and mantissa), e.g. (4, 8) for magnitudes between 1/8 and 3.75, so that the latent
+    has a realistic spread when the scale is 1."""
     n = num_blocks * block_size
-    codes = rng.integers(0, 254, size=(n, 512), dtype=np.uint16)
-    codes = np.where(codes >= 0x7F, codes + 1, codes).astype(np.uint8)      # skip 0x7F; 0xFF is never drawn
+    if code_exp is None:
+        codes = rng.integers(0, 254, size=(n, 512), dtype=np.uint16)
+        codes = np.where(codes >= 0x7F, codes + 1, codes).astype(np.uint8)      # skip 0x7F; 0xFF is never drawn
+    else:
+        sign = rng.integers(0, 2, size=(n, 512), dtype=np.uint16) << 7
+        expo = rng.integers(code_exp[0], min(code_exp[1], 14) + 1, size=(n, 512), dtype=np.uint16) << 3
+        mant = rng.integers(0, 8, size=(n, 512), dtype=np.uint16)
+        codes = (sign | expo | mant).astype(np.uint8)
     rope = _normal_bf16(rng, (n, 64)).view(np.uint8).reshape(n, 128)
     scales = rng.integers(scale_exp[0], scale_exp[1] + 1, size=(n, 8)).astype(np.uint8)
     return np.concatenate([codes, rope, scales], axis=1).reshape(num_blocks, block_size, 648)

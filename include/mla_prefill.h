@@ -96,6 +96,11 @@ typedef struct mla_plan* mla_plan_t;
  *       on this stream; runs on other streams must be ordered after it.
  * On success *out owns a device workspace (work list + status word) until
  * mla_plan_destroy.  Rows that see no key produce O = 0 and LSE = -inf.
+ * A kernel pipeline wait gives up after 2 s (status MLA_ERR_DEVICE_TIMEOUT).  Test
+ * mode: if the environment variable MLA_TEST_FORCE_TIMEOUT_NS holds a value in
+ * 1 .. 2000000000 when the plan is made, its runs make one wait that nothing
+ * satisfies, with that limit, so that tests can drive the time-out path (the kernel
+ * gives up, records MLA_DEVSTAT_TIMEOUT, releases its resources and returns).
  */
 MLA_API int mla_prefill_plan(mla_plan_t* out, const int32_t* qo_indptr, const int32_t* kv_indptr,
                      int batch, int num_heads, int head_dim_qk, int head_dim_vo, int causal,
@@ -141,7 +146,13 @@ MLA_API int mla_prefill_run_merge(mla_plan_t plan, const void* q, const void* k,
  */
 MLA_API int mla_prefill_status(mla_plan_t plan);
 
-/* Release the plan and its workspace (synchronises the device).  NULL is a no-op. */
+/*
+ * Release the plan and its workspace.  Does not synchronise: the workspace goes back
+ * to the device's stream-ordered memory pool once the plan's last use has completed
+ * (the plan upload, and the last run enqueued on a stream that was not being
+ * captured).  A plan whose run was captured into a CUDA graph must outlive every
+ * launch of that graph.  NULL is a no-op.
+ */
 MLA_API int mla_plan_destroy(mla_plan_t plan);
 
 /* Plan facts: which = 0 work units, 1 CTAs launched, 2 total query rows,
@@ -186,6 +197,30 @@ MLA_API int mla_gather_latent(const void* cache, int64_t num_blocks, int block_s
                       int64_t total_tokens, void* out, int32_t* status, void* stream);
 
 /* ======================================================================
+ * Paged gather of an fp8 latent cache, dequantized.  [vLLM-V4] cache dtype
+ * fp8_ds_mla: an fp8 NoPE part, 128 bytes of bf16 RoPE and 8 scale bytes per
+ * token; here for [sglang]'s 512 latent + 64 rope.
+ * ====================================================================== */
+/*
+ *   cache        : uint8 [num_blocks, block_size, entry_bytes], entry_bytes must be 648
+ *                  (MLA_ERR_UNSUPPORTED otherwise): bytes [0, 512) the latent as float8
+ *                  e4m3 (no infinities; 0x7F/0xFF are NaN), [512, 640) the rope as 64 bf16,
+ *                  [640, 648) scale bytes, scale g = 2^(byte_g - 127) covering latent
+ *                  values [64 g, 64 g + 64) (byte 255 is NaN).  8-byte aligned.
+ *   block_table, max_blocks_per_req, cu_seq_lens, chunk_starts, batch, total_tokens,
+ *   status       : as for mla_gather_latent.
+ *   out          : bf16 [total_tokens, 576]: value i < 512 is e4m3(byte_i) * scale_(i/64)
+ *                  rounded to bf16 (round to nearest even; exact unless below bf16's
+ *                  normal range or above its largest value), values 512 .. 575 the rope
+ *                  bits copied.  Rows whose block is unknown are zeros (flagged).
+ * Allocates nothing.
+ */
+MLA_API int mla_gather_latent_fp8(const void* cache, int64_t num_blocks, int block_size, int entry_bytes,
+                                  const int32_t* block_table, int max_blocks_per_req, const int32_t* cu_seq_lens,
+                                  const int32_t* chunk_starts, int batch, int64_t total_tokens, void* out,
+                                  int32_t* status, void* stream);
+
+/* ======================================================================
  * Paged latent cache write.  [sglang] ragged prefill saves the new tokens'
  * compressed rows (512 latent + 64 rope) in the cache before attention;
  * [vLLM-V4] a token's flat slot is block * block_size + offset, and a
@@ -223,6 +258,32 @@ MLA_API int mla_cache_write(void* cache, int64_t num_blocks, int block_size, int
  */
 MLA_API int mla_up_proj(const void* latent, const void* w_kvb, int64_t num_tokens, int num_heads,
                 void* k_out, void* v_out, int32_t* status, void* stream);
+
+/* ======================================================================
+ * Paged up-projection: gather + up-projection in one kernel.  [sglang] asks
+ * whether the compressed kv is decompressed every time; this decompresses a
+ * prefix chunk straight out of the paged cache ([vLLM-V4] slot rule), without
+ * a gathered latent buffer.
+ * ====================================================================== */
+/*
+ * Same result, bit for bit, as mla_gather_latent into a [total_tokens, 576]
+ * buffer followed by mla_up_proj on it:
+ *   cache        : bf16 [num_blocks, block_size, entry_dim]; entry_dim must be 576
+ *                  (MLA_ERR_UNSUPPORTED otherwise); num_blocks * block_size < 2^31 - 1
+ *   block_table, max_blocks_per_req, cu_seq_lens, chunk_starts, batch, total_tokens :
+ *                  as for mla_gather_latent (DEVICE int32 tables; chunk row
+ *                  cu_seq_lens[r] + t is prefix position chunk_starts[r] + t of request r)
+ *   w_kvb        : bf16 [512, num_heads * 256], as for mla_up_proj
+ *   k_out, v_out : bf16 [total_tokens, num_heads, 192] / [total_tokens, num_heads, 128]
+ *   status       : DEVICE int32 word or NULL; MLA_DEVSTAT_BAD_INDEX is OR-ed in when a
+ *                  row's block is unknown (that row's latent is taken as zeros, so its
+ *                  K_nope, V and rope are zero); MLA_DEVSTAT_TIMEOUT as for mla_up_proj.
+ * Allocates nothing.
+ */
+MLA_API int mla_up_proj_paged(const void* cache, int64_t num_blocks, int block_size, int entry_dim,
+                              const int32_t* block_table, int max_blocks_per_req, const int32_t* cu_seq_lens,
+                              const int32_t* chunk_starts, int batch, int64_t total_tokens, const void* w_kvb,
+                              int num_heads, void* k_out, void* v_out, int32_t* status, void* stream);
 
 /* ======================================================================
  * LSE merge of two partial attention states.  [vLLM-FI]

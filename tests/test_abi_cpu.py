@@ -156,3 +156,29 @@ def test_planner_units_grouped_by_request_head_early():
     first = units[offs[:-1]]
     groups = {(int(u[0]), int(np.searchsorted(qo, u[1], side="right") - 1)) for u in first}
     assert len(groups) <= 8
+
+
+def test_bindings_check_shapes_before_any_call():
+    """The Python wrappers reject outputs of the wrong size before the library sees a
+    pointer (the C side gets raw pointers and would write past a short buffer)."""
+    import torch
+    from chunked_prefill_attention_ragged_gb300 import _binding
+    qo = np.array([0, 40, 60], dtype=np.int32)
+    bf = torch.bfloat16
+    q, k, v = torch.zeros(60, 4, 192, dtype=bf), torch.zeros(60, 4, 192, dtype=bf), torch.zeros(60, 4, 128, dtype=bf)
+    with pytest.raises(ValueError):   # O one row short
+        _binding.mla_prefill_run_noalloc(qo, qo, 4, q, k, v, torch.zeros(59, 4, 128, dtype=bf), sm_scale=0.1)
+    with pytest.raises(ValueError):   # LSE of the wrong shape
+        _binding.mla_prefill_run_noalloc(qo, qo, 4, q, k, v, torch.zeros(60, 4, 128, dtype=bf),
+                                         torch.zeros(60, 3), sm_scale=0.1)
+    with pytest.raises(ValueError):   # kv_indptr shorter than qo_indptr
+        _binding.mla_prefill_run_noalloc(qo, qo[:2], 4, q, k, v, torch.zeros(60, 4, 128, dtype=bf), sm_scale=0.1)
+    with pytest.raises(ValueError):   # V with the wrong head dim
+        _binding.mla_prefill_run_noalloc(qo, qo, 4, q, k, torch.zeros(60, 4, 192, dtype=bf),
+                                         torch.zeros(60, 4, 128, dtype=bf), sm_scale=0.1)
+    oa = torch.zeros(10, 2, 128, dtype=bf)
+    la = torch.zeros(10, 2)
+    with pytest.raises(ValueError):   # merge: o_b smaller than o_a
+        _binding.mla_merge_state(oa, la, torch.zeros(9, 2, 128, dtype=bf), la)
+    with pytest.raises(ValueError):   # merge: lse_b of the wrong shape
+        _binding.mla_merge_state(oa, la, oa, torch.zeros(10, 3))

@@ -4,7 +4,7 @@ import pytest
 
 from chunked_prefill_attention_ragged_gb300 import workloads as wl
 from oracle import chunked_prefill_attention
-from gpu_util import check_attention, f64_of_bf16, sample_rows, to_dev, to_dev_bf16
+from gpu_util import Guarded, check_attention, chunked_oracle_parallel, f64_of_bf16, sample_rows, to_dev, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -15,10 +15,15 @@ def run_pipeline(cb: wl.ChunkedPrefixBatch, fuse_merge=True):
     b = cb.new
     pipe = ChunkedPrefill(b.qo_indptr, cb.layout.cu_seq_lens, cb.layout.chunk_starts, b.num_heads,
                           sm_scale=b.sm_scale, logits_soft_cap=b.logits_soft_cap, fuse_merge=fuse_merge)
+    rows = b.q.shape[0]
+    g_o = Guarded((rows, b.num_heads, 128), torch.bfloat16)
+    g_l = Guarded((rows, b.num_heads), torch.float32)
     o, lse = pipe.run(to_dev_bf16(b.q), to_dev_bf16(b.k), to_dev_bf16(b.v), to_dev_bf16(cb.cache),
-                      to_dev(cb.block_table), to_dev_bf16(cb.w_kvb))
+                      to_dev(cb.block_table), to_dev_bf16(cb.w_kvb), o=g_o.tensor, lse=g_l.tensor)
     torch.cuda.synchronize()
     pipe.check_status()
+    g_o.check("pipeline O")
+    g_l.check("pipeline LSE")
     return o, lse
 
 
@@ -35,17 +40,15 @@ def test_small_chunked_full(cap, fuse):
 
 
 def test_workload2_sampled():
+    """4 x (2048 new + 8192 cached), all 128 heads, on a row sample: first 2, last 2, every
+    128-row tile boundary +-1 and 512 seeded random rows per request."""
     cb = wl.make_chunked_prefix()
     o, lse = run_pipeline(cb)
     b = cb.new
-    rows = sample_rows(b.q_lens, n_random=16, every_tile=4, seed=2)
-    heads = [0, 127]
-    o_ref, lse_ref = chunked_prefill_attention(b.q, b.k, b.v, b.qo_indptr, cb.cache, cb.block_table,
-                                               cb.prefix_lens, cb.w_kvb, sm_scale=b.sm_scale, rows=rows,
-                                               heads=heads)
+    rows = sample_rows(b.q_lens, n_random=512, every_tile=1, seed=2)
+    o_ref, lse_ref = chunked_oracle_parallel(cb, rows)
     idx = torch.from_numpy(np.concatenate([b.qo_indptr[r] + rows[r] for r in range(b.batch)])).cuda()
-    check_attention(f64_of_bf16(o[idx][:, heads]), lse[idx][:, heads].double().cpu().numpy(), o_ref, lse_ref,
-                    "workload2")
+    check_attention(f64_of_bf16(o[idx]), lse[idx].double().cpu().numpy(), o_ref, lse_ref, "workload2")
 
 
 def test_all_chunk_gather_matches_oracle_per_chunk():
@@ -109,3 +112,49 @@ def test_run_merge_requires_lse():
     assert rc == -1
     with pytest.raises(ValueError):
         plan.run_merge(q, k, v, o, None)
+
+
+def test_small_chunked_fp8_cache_full():
+    """The pipeline over an fp8 latent cache (dequantizing gather -> up-projection -> chunk
+    attention merged into the new tokens' state) against the unchunked oracle over the
+    oracle's dequantization of the same cache."""
+    from chunked_prefill_attention_ragged_gb300.pipeline import ChunkedPrefill
+    from oracle import dequant_fp8_entries
+    cb = wl.random_chunked_prefix(23, [130, 5, 260], [300, 0, 1000], 4, num_blocks=64, block_size=64,
+                                  chunk_tokens=256)
+    cache8 = wl.random_fp8_cache(np.random.default_rng(24), 64, 64, scale_exp=(126, 127), code_exp=(4, 8))
+    b = cb.new
+    pipe = ChunkedPrefill(b.qo_indptr, cb.layout.cu_seq_lens, cb.layout.chunk_starts, b.num_heads,
+                          sm_scale=b.sm_scale, cache_fp8=True)
+    o, lse = pipe.run(to_dev_bf16(b.q), to_dev_bf16(b.k), to_dev_bf16(b.v), to_dev(cache8), to_dev(cb.block_table),
+                      to_dev_bf16(cb.w_kvb))
+    torch.cuda.synchronize()
+    pipe.check_status()
+    cache_bf16 = dequant_fp8_entries(cache8.reshape(-1, 648)).reshape(64, 64, 576)
+    o_ref, lse_ref = chunked_prefill_attention(b.q, b.k, b.v, b.qo_indptr, cache_bf16, cb.block_table,
+                                               cb.prefix_lens, cb.w_kvb, sm_scale=b.sm_scale)
+    check_attention(f64_of_bf16(o), lse.double().cpu().numpy(), o_ref, lse_ref, "fp8 cache pipeline")
+
+
+@pytest.mark.parametrize("paged", [True, False])
+def test_small_chunked_paged_and_gathered_agree(paged):
+    """The pipeline with the paged up-projection and with gather + up-projection: both
+    against the oracle (and equal to each other bit for bit, same kernels downstream)."""
+    from chunked_prefill_attention_ragged_gb300.pipeline import ChunkedPrefill
+    cb = wl.random_chunked_prefix(25, [77, 200], [500, 129], 3, num_blocks=16, block_size=64, chunk_tokens=192)
+    b = cb.new
+    outs = []
+    for pg in (True, False):
+        pipe = ChunkedPrefill(b.qo_indptr, cb.layout.cu_seq_lens, cb.layout.chunk_starts, b.num_heads,
+                              sm_scale=b.sm_scale, paged_up_proj=pg)
+        o, lse = pipe.run(to_dev_bf16(b.q), to_dev_bf16(b.k), to_dev_bf16(b.v), to_dev_bf16(cb.cache),
+                          to_dev(cb.block_table), to_dev_bf16(cb.w_kvb))
+        torch.cuda.synchronize()
+        pipe.check_status()
+        outs.append((o, lse))
+    assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
+    assert torch.equal(outs[0][1], outs[1][1])
+    o, lse = outs[0 if paged else 1]
+    o_ref, lse_ref = chunked_prefill_attention(b.q, b.k, b.v, b.qo_indptr, cb.cache, cb.block_table, cb.prefix_lens,
+                                               cb.w_kvb, sm_scale=b.sm_scale)
+    check_attention(f64_of_bf16(o), lse.double().cpu().numpy(), o_ref, lse_ref, f"paged={paged}")

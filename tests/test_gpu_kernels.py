@@ -4,7 +4,7 @@ import pytest
 
 from chunked_prefill_attention_ragged_gb300 import workloads as wl
 from oracle import bf16_bits_to_f64, cache_write, gather_latent, merge_state, round_f64_to_bf16, up_project
-from gpu_util import bits_of, f64_of_bf16, to_dev, to_dev_bf16
+from gpu_util import Guarded, bits_of, f64_of_bf16, to_dev, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -24,8 +24,10 @@ def test_gather_workload2_bit_exact():
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     for c in range(cb.layout.num_chunks):
         cu, st = cb.layout.cu_seq_lens[c], cb.layout.chunk_starts[c]
-        out = mla.mla_gather_latent(cache, table, to_dev(cu), to_dev(st), int(cu[-1]), status=status)
+        g = Guarded((int(cu[-1]), 576), torch.bfloat16)
+        out = mla.mla_gather_latent(cache, table, to_dev(cu), to_dev(st), int(cu[-1]), out=g.tensor, status=status)
         torch.cuda.synchronize()
+        g.check("gather")
         np.testing.assert_array_equal(bits_of(out), gather_latent(cb.cache, cb.block_table, cu, st))
     assert int(status.item()) == 0
 
@@ -38,8 +40,10 @@ def test_gather_random_tables(block_size, chunk):
     cache, table = to_dev_bf16(cb.cache), to_dev(cb.block_table)
     for c in range(cb.layout.num_chunks):
         cu, st = cb.layout.cu_seq_lens[c], cb.layout.chunk_starts[c]
-        out = mla.mla_gather_latent(cache, table, to_dev(cu), to_dev(st), int(cu[-1]))
+        g = Guarded((int(cu[-1]), 576), torch.bfloat16)
+        out = mla.mla_gather_latent(cache, table, to_dev(cu), to_dev(st), int(cu[-1]), out=g.tensor)
         torch.cuda.synchronize()
+        g.check("gather")
         np.testing.assert_array_equal(bits_of(out), gather_latent(cb.cache, cb.block_table, cu, st))
 
 
@@ -75,8 +79,10 @@ def test_gather_row_widths(entry_dim):
     table = rng.permutation(num_blocks)[:6].reshape(2, 3).astype(np.int32)
     cu = np.array([0, 9, 19], dtype=np.int32)
     st = np.array([1, 0], dtype=np.int32)
-    out = mla.mla_gather_latent(to_dev_bf16(cache), to_dev(table), to_dev(cu), to_dev(st), int(cu[-1]))
+    g = Guarded((int(cu[-1]), entry_dim), torch.bfloat16)
+    out = mla.mla_gather_latent(to_dev_bf16(cache), to_dev(table), to_dev(cu), to_dev(st), int(cu[-1]), out=g.tensor)
     torch.cuda.synchronize()
+    g.check("gather")
     np.testing.assert_array_equal(bits_of(out), gather_latent(cache, table, cu, st))
 
 
@@ -99,10 +105,13 @@ def test_cache_write_bit_exact(entry_dim, tokens, pad):
     cache = rng.integers(0, 1 << 16, size=(nb, bs, entry_dim), dtype=np.uint16)
     lat = rng.integers(0, 1 << 16, size=(tokens, entry_dim), dtype=np.uint16)
     slots = _slots(rng, tokens, nb * bs, pad)
-    d_cache = to_dev_bf16(cache)
+    g = Guarded((nb, bs, entry_dim), torch.bfloat16)
+    d_cache = g.tensor
+    d_cache.copy_(to_dev_bf16(cache))
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     mla.mla_cache_write(d_cache, to_dev_bf16(lat), to_dev(slots), status=status)
     torch.cuda.synchronize()
+    g.check("cache write")
     assert int(status.item()) == 0
     np.testing.assert_array_equal(bits_of(d_cache), cache_write(cache, lat, slots))
 
@@ -113,10 +122,13 @@ def test_cache_write_bad_slot_is_flagged_and_skipped():
     cache = rng.integers(0, 1 << 16, size=(4, 16, 576), dtype=np.uint16)
     lat = rng.integers(0, 1 << 16, size=(6, 576), dtype=np.uint16)
     slots = np.array([3, 64, 10, 1000, -5, 63], dtype=np.int64)   # 64 and 1000 are past the cache
-    d_cache = to_dev_bf16(cache)
+    g = Guarded((4, 16, 576), torch.bfloat16)
+    d_cache = g.tensor
+    d_cache.copy_(to_dev_bf16(cache))
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     mla.mla_cache_write(d_cache, to_dev_bf16(lat), to_dev(slots), status=status)
     torch.cuda.synchronize()
+    g.check("cache write with bad slots")
     assert int(status.item()) & 2
     keep = slots.copy()
     keep[(keep >= 64)] = -1
@@ -144,39 +156,47 @@ def test_cache_write_then_gather_round_trip():
 
 
 # ------------------------------------------------------------------ up-projection
-@pytest.mark.parametrize("tokens,heads,out_offset", [(300, 4, 0), (128, 1, 0), (1, 2, 0), (1000, 16, 0),
-                                                     (300, 4, 8), (77, 3, 8)])
-def test_up_proj_matches_rounded_oracle(tokens, heads, out_offset):
-    """out_offset = 8 elements puts K and V 16 but not 32 bytes into their buffers (16-byte stores)."""
-    mla = _mla()
-    rng = np.random.default_rng(tokens + heads)
-    lat = wl.to_bf16_bits(rng.standard_normal((tokens, 576)).astype(np.float32))
-    w = wl.to_bf16_bits((rng.standard_normal((512, heads * 256)) * 512 ** -0.5).astype(np.float32))
-    k_buf = torch.full((out_offset + tokens * heads * 192,), float("nan"), dtype=torch.bfloat16, device="cuda")
-    v_buf = torch.full((out_offset + tokens * heads * 128,), float("nan"), dtype=torch.bfloat16, device="cuda")
-    k_out = k_buf[out_offset:].view(tokens, heads, 192)
-    v_out = v_buf[out_offset:].view(tokens, heads, 128)
-    k, v = mla.mla_up_proj(to_dev_bf16(lat), to_dev_bf16(w), heads, k_out=k_out, v_out=v_out)
-    torch.cuda.synchronize()
-    assert bool(torch.isnan(k_buf[:out_offset]).all()) and bool(torch.isnan(v_buf[:out_offset]).all())
+def _check_up_proj(lat, w, heads, k, v):
+    """Element-wise: one bf16 rounding of a value that fp32 accumulation may have moved by
+    at most 512 * 2^-23 * sum|latent * W|; the rope part is a bit-exact copy."""
     k_ref, v_ref = up_project(lat, w, heads)
-    # Worst-case fp32 accumulation error of a 512-term dot product, per output element.
     a = np.abs(bf16_bits_to_f64(lat[:, :512]))
-    wa = np.abs(bf16_bits_to_f64(w)).reshape(512, heads, 256)
-    mag = np.einsum("tc,chd->thd", a, wa)
+    wa = np.abs(bf16_bits_to_f64(w))
+    mag = (a @ wa).reshape(lat.shape[0], heads, 256)
     acc_bound = 512 * 2.0 ** -23 * mag
     kg, vg = f64_of_bf16(k), f64_of_bf16(v)
-    # rope part is a copy: bit-exact
     np.testing.assert_array_equal(kg[:, :, 128:], k_ref[:, :, 128:])
     for got, ref, bound, what in ((kg[:, :, :128], k_ref[:, :, :128], acc_bound[..., :128], "K_nope"),
                                   (vg, v_ref, acc_bound[..., 128:], "V")):
         rref = round_f64_to_bf16(ref)
         ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -126))) - 7)
-        # one bf16 rounding of a value that fp32 accumulation may have moved by `bound`
         err = np.abs(got - ref)
         worst = np.max(err / (ulp + bound))
         assert worst <= 1.0, f"{what}: error {worst:.3f} x (ulp + accumulation bound)"
         assert np.mean(got != rref) < 0.02, f"{what}: {np.mean(got != rref):.4f} differ from exact rounding"
+
+
+@pytest.mark.parametrize("tokens,heads,out_offset", [(300, 4, 0), (128, 1, 0), (1, 2, 0), (1000, 16, 0),
+                                                     (300, 4, 8), (77, 3, 8), (2048, 128, 0), (1100, 37, 0)])
+def test_up_proj_matches_rounded_oracle(tokens, heads, out_offset):
+    """out_offset = 8 elements puts K and V 16 but not 32 bytes into their buffers (16-byte
+    stores).  2048 x 128 heads is 2048 tiles, over 13 per CTA: every CTA's range crosses
+    token blocks (the latent tile reloaded in mid-range) and reuses both TMEM
+    accumulators; 1100 x 37 gives ranges that start and end inside a token block."""
+    mla = _mla()
+    rng = np.random.default_rng(tokens + heads)
+    lat = wl.to_bf16_bits(rng.standard_normal((tokens, 576)).astype(np.float32))
+    w = wl.to_bf16_bits((rng.standard_normal((512, heads * 256)) * 512 ** -0.5).astype(np.float32))
+    g_k = Guarded((out_offset + tokens * heads * 192,), torch.bfloat16, fill=float("nan"))
+    g_v = Guarded((out_offset + tokens * heads * 128,), torch.bfloat16, fill=float("nan"))
+    k_out = g_k.tensor[out_offset:].view(tokens, heads, 192)
+    v_out = g_v.tensor[out_offset:].view(tokens, heads, 128)
+    k, v = mla.mla_up_proj(to_dev_bf16(lat), to_dev_bf16(w), heads, k_out=k_out, v_out=v_out)
+    torch.cuda.synchronize()
+    g_k.check("up-projection K")
+    g_v.check("up-projection V")
+    assert bool(torch.isnan(g_k.tensor[:out_offset]).all()) and bool(torch.isnan(g_v.tensor[:out_offset]).all())
+    _check_up_proj(lat, w, heads, k, v)
 
 
 # ------------------------------------------------------------------ merge
@@ -199,8 +219,11 @@ def _merge_inputs(rows, heads, seed, dim=128):
 def test_merge_matches_oracle(rows, heads, dim):
     mla = _mla()
     oa, la, ob, lb = _merge_inputs(rows, heads, rows, dim)
-    o, l = mla.mla_merge_state(to_dev_bf16(oa), to_dev(la), to_dev_bf16(ob), to_dev(lb))
+    g_o, g_l = Guarded((rows, heads, dim), torch.bfloat16), Guarded((rows, heads), torch.float32)
+    o, l = mla.mla_merge_state(to_dev_bf16(oa), to_dev(la), to_dev_bf16(ob), to_dev(lb), g_o.tensor, g_l.tensor)
     torch.cuda.synchronize()
+    g_o.check("merge O")
+    g_l.check("merge LSE")
     o_ref, l_ref = merge_state(oa, la.astype(np.float64), ob, lb.astype(np.float64))
     og = f64_of_bf16(o)
     assert np.abs(og - o_ref).max() <= 2.0 ** -8 * np.abs(o_ref).max() + 1e-6
@@ -222,3 +245,157 @@ def test_merge_in_place():
     torch.cuda.synchronize()
     assert torch.equal(ta.view(torch.int16), o_sep.view(torch.int16))
     assert torch.equal(tla, l_sep)
+
+
+# ------------------------------------------------------------------ paged up-projection
+def test_up_proj_paged_bit_identical_to_gather_then_up_proj_workload2():
+    """Both chunks of the chunked-prefix workload (16384 rows x 128 heads each): the fused
+    kernel equals the gather followed by the up-projection, bit for bit."""
+    mla = _mla()
+    cb = wl.make_chunked_prefix()
+    cache, table, w = to_dev_bf16(cb.cache), to_dev(cb.block_table), to_dev_bf16(cb.w_kvb)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    H = cb.new.num_heads
+    for c in range(cb.layout.num_chunks):
+        cu, st = to_dev(cb.layout.cu_seq_lens[c]), to_dev(cb.layout.chunk_starts[c])
+        t = int(cb.layout.cu_seq_lens[c][-1])
+        lat = mla.mla_gather_latent(cache, table, cu, st, t, status=status)
+        k_ref, v_ref = mla.mla_up_proj(lat, w, H, status=status)
+        g_k, g_v = Guarded((t, H, 192), torch.bfloat16), Guarded((t, H, 128), torch.bfloat16)
+        k, v = mla.mla_up_proj_paged(cache, table, cu, st, t, w, H, g_k.tensor, g_v.tensor, status=status)
+        torch.cuda.synchronize()
+        g_k.check("paged K")
+        g_v.check("paged V")
+        assert int(status.item()) == 0
+        assert torch.equal(k.view(torch.int16), k_ref.view(torch.int16)), f"chunk {c}: K differs"
+        assert torch.equal(v.view(torch.int16), v_ref.view(torch.int16)), f"chunk {c}: V differs"
+        del lat, k_ref, v_ref, k, v, g_k, g_v
+
+
+@pytest.mark.parametrize("n_req,block_size,chunk,heads", [(3, 64, 300, 4), (3, 16, 100, 2), (40, 1, 37, 2),
+                                                         (5, 64, 4096, 3)])
+def test_up_proj_paged_matches_oracle(n_req, block_size, chunk, heads):
+    """Random tables and ragged chunk layouts (rows of a token block from several requests,
+    chunk starts not aligned to blocks, more than 31 requests), against the oracle's
+    gather followed by its up-projection, element-wise."""
+    mla = _mla()
+    rng = np.random.default_rng(n_req * 1000 + block_size)
+    prefix = rng.integers(0, 700, size=n_req)
+    prefix[0] = 0
+    nb = int(sum(-(-int(p) // block_size) for p in prefix)) + 5
+    cb = wl.random_chunked_prefix(int(rng.integers(1 << 30)), [1] * n_req, prefix, heads, num_blocks=nb,
+                                  block_size=block_size, chunk_tokens=chunk)
+    cache, table, w = to_dev_bf16(cb.cache), to_dev(cb.block_table), to_dev_bf16(cb.w_kvb)
+    for c in range(cb.layout.num_chunks):
+        cu, st = cb.layout.cu_seq_lens[c], cb.layout.chunk_starts[c]
+        t = int(cu[-1])
+        if t == 0:
+            continue
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        k, v = mla.mla_up_proj_paged(cache, table, to_dev(cu), to_dev(st), t, w, heads, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        lat = gather_latent(cb.cache, cb.block_table, cu, st)
+        _check_up_proj(lat, cb.w_kvb, heads, k, v)
+
+
+def test_up_proj_paged_bad_block_gives_zero_rows_and_flag():
+    mla = _mla()
+    cb = wl.random_chunked_prefix(6, [1, 1], [150, 130], 2, num_blocks=8, block_size=64, chunk_tokens=256)
+    table = cb.block_table.copy()
+    table[1, 1] = 99                     # outside the cache: request 1, positions 64..127
+    cu, st = cb.layout.cu_seq_lens[0], cb.layout.chunk_starts[0]
+    t = int(cu[-1])
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    k, v = mla.mla_up_proj_paged(to_dev_bf16(cb.cache), to_dev(table), to_dev(cu), to_dev(st), t,
+                                 to_dev_bf16(cb.w_kvb), 2, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 2
+    bad = np.arange(cu[1] + 64, cu[1] + 128)
+    kb, vb = bits_of(k), bits_of(v)
+    assert not kb[bad].any() and not vb[bad].any()
+    good = np.setdiff1d(np.arange(t), bad)
+    lat = gather_latent(cb.cache, cb.block_table, cu, st)
+    k_ref, v_ref = up_project(lat, cb.w_kvb, 2)
+    np.testing.assert_array_equal(f64_of_bf16(k)[good][:, :, 128:], k_ref[good][:, :, 128:])
+    assert np.abs(f64_of_bf16(v)[good] - v_ref[good]).max() < 0.05
+
+
+# ------------------------------------------------------------------ fp8 latent cache
+def _fp8_gather(mla, cache, table, cu, st, status=None):
+    t = int(cu[-1])
+    g = Guarded((t, 576), torch.bfloat16)
+    out = mla.mla_gather_latent_fp8(to_dev(cache), to_dev(table), to_dev(cu), to_dev(st), t, out=g.tensor,
+                                    status=status)
+    torch.cuda.synchronize()
+    g.check("fp8 gather")
+    return bits_of(out)
+
+
+@pytest.mark.parametrize("n_req,block_size,chunk", [(4, 64, 4096), (3, 16, 100), (40, 1, 37), (5, 64, 333)])
+def test_gather_fp8_bit_exact(n_req, block_size, chunk):
+    from oracle import gather_latent_fp8
+    mla = _mla()
+    rng = np.random.default_rng(n_req * 7 + block_size)
+    prefix = rng.integers(1, 900, size=n_req)
+    nb = int(sum(-(-int(p) // block_size) for p in prefix)) + 3
+    cache = wl.random_fp8_cache(rng, nb, block_size)
+    perm = rng.permutation(nb).astype(np.int32)
+    per = [-(-int(p) // block_size) for p in prefix]
+    table = np.full((n_req, max(per)), -1, dtype=np.int32)
+    pos = 0
+    for r, k in enumerate(per):
+        table[r, :k] = perm[pos:pos + k]
+        pos += k
+    lay = wl.chunk_layout(prefix, chunk)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for c in range(lay.num_chunks):
+        cu, st = lay.cu_seq_lens[c], lay.chunk_starts[c]
+        if cu[-1] == 0:
+            continue
+        got = _fp8_gather(mla, cache, table, cu, st, status)
+        np.testing.assert_array_equal(got, gather_latent_fp8(cache, table, cu, st))
+    assert int(status.item()) == 0
+
+
+def test_gather_fp8_extreme_scales_and_nan_codes():
+    """Scales at the ends of the range (bf16 subnormal results, overflow to infinity), NaN
+    fp8 codes and NaN scales: every finite result bit-exact, NaN exactly where the oracle
+    has NaN."""
+    from oracle import gather_latent_fp8
+    mla = _mla()
+    rng = np.random.default_rng(77)
+    cache = wl.random_fp8_cache(rng, 8, 16, scale_exp=(0, 6))
+    cache[4:] = wl.random_fp8_cache(rng, 4, 16, scale_exp=(245, 254))
+    flat = cache.reshape(-1, 648)
+    flat[::7, 5] = 0x7F            # NaN codes
+    flat[::11, 300] = 0xFF
+    flat[3, 641] = 0xFF            # a NaN scale
+    table = np.arange(8, dtype=np.int32).reshape(2, 4)
+    cu = np.array([0, 64, 128], dtype=np.int32)
+    st = np.array([0, 0], dtype=np.int32)
+    got = _fp8_gather(mla, cache, table, cu, st)
+    ref = gather_latent_fp8(cache, table, cu, st)
+    g_nan = (got & 0x7FFF) > 0x7F80
+    r_nan = (ref & 0x7FFF) > 0x7F80
+    np.testing.assert_array_equal(g_nan, r_nan)
+    np.testing.assert_array_equal(got[~r_nan], ref[~r_nan])
+    assert r_nan.any() and (ref == 0x7F80).any() and ((ref & 0x7F80) == 0).any()   # NaN, inf, subnormal/zero seen
+
+
+def test_gather_fp8_bad_block_flags_and_zeroes():
+    from oracle import gather_latent_fp8
+    mla = _mla()
+    rng = np.random.default_rng(78)
+    cache = wl.random_fp8_cache(rng, 4, 64)
+    table = np.array([[0, 1], [2, 99]], dtype=np.int32)
+    cu = np.array([0, 70, 140], dtype=np.int32)
+    st = np.array([0, 0], dtype=np.int32)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = _fp8_gather(mla, cache, table, cu, st, status)
+    assert int(status.item()) & 2
+    bad = np.arange(70 + 64, 140)
+    assert not got[bad].any()
+    good_table = np.array([[0, 1], [2, 3]], dtype=np.int32)
+    keep = np.setdiff1d(np.arange(140), bad)
+    np.testing.assert_array_equal(got[keep], gather_latent_fp8(cache, good_table, cu, st)[keep])
