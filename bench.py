@@ -810,6 +810,44 @@ def bench_reference(args, world, rank):
     }
 
 
+def kernel_case(name: str, reps: int = 3):
+    """A small case of one kernel, launched `reps` times and nothing else: the command that
+    the ncu captures under profiles/ run (``--kernel-case``)."""
+    import torch
+    import chunked_prefill_attention_ragged_gb300 as mla
+    from chunked_prefill_attention_ragged_gb300.pipeline import ChunkedPrefill
+    dev = torch.device("cuda", 0)
+    cb = wl.make_chunked_prefix()
+    table = torch.from_numpy(cb.block_table).to(dev)
+
+    def dev_bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    if name == "fp8_gather":
+        # every chunk of the chunked-prefix workload out of an fp8 cache of the same shape
+        b = cb.new
+        pipe = ChunkedPrefill(b.qo_indptr, cb.layout.cu_seq_lens, cb.layout.chunk_starts, b.num_heads,
+                              sm_scale=b.sm_scale, device=dev, cache_fp8=True)
+        cache8 = torch.from_numpy(wl.random_fp8_cache(np.random.default_rng(1102), cb.cache.shape[0],
+                                                      cb.cache.shape[1], scale_exp=(126, 127),
+                                                      code_exp=(4, 8))).to(dev)
+        for _ in range(reps):
+            pipe.gather_all(cache8, table)
+    elif name == "up_proj_paged":
+        # the first 1024 prefix positions of each request: 4096 rows x 128 heads (335 MB of K/V)
+        cache, w = dev_bf16(cb.cache), dev_bf16(cb.w_kvb)
+        cu = torch.tensor([0, 1024, 2048, 3072, 4096], dtype=torch.int32, device=dev)
+        st = torch.zeros(4, dtype=torch.int32, device=dev)
+        k = torch.empty(4096, 128, 192, dtype=torch.bfloat16, device=dev)
+        v = torch.empty(4096, 128, 128, dtype=torch.bfloat16, device=dev)
+        for _ in range(reps):
+            mla.mla_up_proj_paged(cache, table, cu, st, 4096, w, 128, k, v)
+    else:
+        raise ValueError(name)
+    torch.cuda.synchronize()
+    print(json.dumps({"kernel_case": name, "launches": reps, "ok": True}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -821,7 +859,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-chunked", action="store_true")
     ap.add_argument("--no-workloads", action="store_true", help="skip the rows of the other workloads")
+    ap.add_argument("--kernel-case", choices=["fp8_gather", "up_proj_paged"], default=None,
+                    help="launch one kernel on a small case and exit (for profiler captures)")
     args = ap.parse_args()
+    if args.kernel_case:
+        kernel_case(args.kernel_case)
+        return
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_env()
     if args.impl == "reference":

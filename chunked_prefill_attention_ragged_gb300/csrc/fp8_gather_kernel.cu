@@ -9,11 +9,14 @@
 // pos % block_size).
 //
 // Memory bound (648 bytes read, 1152 written per token).  One warp per row at a time:
-// lane l converts latent values 16 l .. 16 l + 15 (group l / 4) with the hardware e4m3x2
-// -> f16x2 conversion (exact), one fp32 multiply by the scale (exact: a 4-bit significand
-// times a power of two) and one rounding to bf16, and stores 32 contiguous bytes; lanes
-// 0-15 copy the rope.  Each warp issues the loads of several rows before converting any,
-// to keep enough bytes in flight.
+// lane l converts latent values 8 l .. 8 l + 7 and 256 + 8 l .. 256 + 8 l + 7 (scale
+// groups l / 8 and 4 + l / 8) with the hardware e4m3x2 -> f16x2 conversion (exact), one
+// fp32 multiply by the scale (exact: a 4-bit significand times a power of two) and one
+// rounding to bf16, so that each warp-wide load reads 256 contiguous bytes and each
+// warp-wide store writes 512; lanes 0-15 copy the rope.  The grid is exactly one wave of
+// resident warps (grid-stride over rows, two rows in flight per warp): with one row batch
+// per warp and as many warps as batches, the second, partial wave of a 75 MB gather left
+// most SMs idle.
 #include "internal.h"
 #include "paged.cuh"
 #include "ptx.cuh"
@@ -22,7 +25,8 @@ namespace mla {
 namespace {
 
 constexpr int kEntry = 648;
-constexpr int kRowsPerWarp = 4;
+constexpr int kRowsPerWarp = 2;
+constexpr int kBlocksPerSm = 6;   // 48 warps per SM, every one resident from the start
 constexpr int kThreads = 256;
 
 __device__ __forceinline__ uint2 ld_nc_u2(const uint8_t* p) {
@@ -50,7 +54,7 @@ __device__ __forceinline__ uint32_t dequant2(uint32_t two_fp8, float scale) {
   return pack_bf16x2(xl, xh);
 }
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kBlocksPerSm)
 gather_fp8_kernel(const uint8_t* __restrict__ cache, RowMap m, int64_t total_rows, uint8_t* __restrict__ out,
                   int32_t* status) {
   const int lane = threadIdx.x & 31;
@@ -71,8 +75,8 @@ gather_fp8_kernel(const uint8_t* __restrict__ cache, RowMap m, int64_t total_row
       lat[u][0] = lat[u][1] = rope[u] = sc[u] = make_uint2(0, 0);
       if (have[u]) {
         const uint8_t* src = cache + slot * kEntry;
-        lat[u][0] = ld_nc_u2(src + lane * 16);
-        lat[u][1] = ld_nc_u2(src + lane * 16 + 8);
+        lat[u][0] = ld_nc_u2(src + lane * 8);
+        lat[u][1] = ld_nc_u2(src + 256 + lane * 8);
         sc[u] = ld_nc_u2(src + 640);
         if (lane < 16) rope[u] = ld_nc_u2(src + 512 + lane * 8);
       }
@@ -84,22 +88,22 @@ gather_fp8_kernel(const uint8_t* __restrict__ cache, RowMap m, int64_t total_row
       uint8_t* dst = out + row * (576 * 2);
       uint32_t w[8];
       if (have[u]) {
-        const int g = lane >> 2;   // the scale of latent values 16 lane .. 16 lane + 15
-        const uint32_t sbyte = ((g < 4 ? sc[u].x : sc[u].y) >> (8 * (g & 3))) & 0xFFu;
-        const float scale = ue8m0_scale(sbyte);
+        // values 8 lane ..: group lane / 8 (scale bytes 0-3); 256 + 8 lane ..: group 4 + lane / 8
+        const int sh = 8 * (lane >> 3);
+        const float s0 = ue8m0_scale((sc[u].x >> sh) & 0xFFu), s1 = ue8m0_scale((sc[u].y >> sh) & 0xFFu);
         const uint32_t src[4] = {lat[u][0].x, lat[u][0].y, lat[u][1].x, lat[u][1].y};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          w[2 * q] = dequant2(src[q] & 0xFFFFu, scale);
-          w[2 * q + 1] = dequant2(src[q] >> 16, scale);
+          const float sq = q < 2 ? s0 : s1;
+          w[2 * q] = dequant2(src[q] & 0xFFFFu, sq);
+          w[2 * q + 1] = dequant2(src[q] >> 16, sq);
         }
       } else {
 #pragma unroll
         for (int q = 0; q < 8; ++q) w[q] = 0;
       }
-      uint4* d4 = reinterpret_cast<uint4*>(dst + lane * 32);
-      d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      reinterpret_cast<uint4*>(dst)[lane] = make_uint4(w[0], w[1], w[2], w[3]);
+      reinterpret_cast<uint4*>(dst + 512)[lane] = make_uint4(w[4], w[5], w[6], w[7]);
       if (lane < 16) *reinterpret_cast<uint2*>(dst + 1024 + lane * 8) = rope[u];
     }
   }
@@ -114,7 +118,7 @@ cudaError_t launch_gather_fp8(const void* cache, int64_t num_blocks, int block_s
   const int sms = device_sm_count();
   const int64_t warps_needed = (total_tokens + kRowsPerWarp - 1) / kRowsPerWarp;
   const int64_t blocks_needed = (warps_needed + kThreads / 32 - 1) / (kThreads / 32);
-  const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 8;
+  const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * kBlocksPerSm;
   const int grid = (int)(blocks_needed < cap ? blocks_needed : cap);
   RowMap m{cu_seq_lens, chunk_starts, block_table, batch, max_blocks_per_req, block_size, num_blocks};
   gather_fp8_kernel<<<grid, kThreads, 0, stream>>>(static_cast<const uint8_t*>(cache), m, total_tokens,
