@@ -23,7 +23,9 @@ computes, written from the pages' definitions:
   * the fp8 latent cache entry (fp8 latent with power-of-two scales per 64
     values, bf16 rope; vLLM ``sparse_mla.py``'s ``fp8_ds_mla`` layout) and its
     dequantizing gather;
-  * the unchunked attention that chunked prefill must reproduce.
+  * the unchunked attention that chunked prefill must reproduce;
+  * absorbed-weight attention (multi-query over the 576-wide compressed rows,
+    sglang issue #3849's forward_absorb; explicit sm_scale per TVM PR #17674).
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  It shares no code with the CUDA path
@@ -36,7 +38,9 @@ closed forms and invariants.  Parity pins: attention (brute force, closed
 forms, invariants), gather (hand fixture + brute force), cache write (hand
 fixture, round trip through the gather, padding slots), up-projection
 (hand fixture + triple loop), merge (closed forms + split/merge identity),
-chunked pipeline (split/merge identity), fp8 entries (hand-decoded codes, every
+chunked pipeline (split/merge identity), absorbed attention (the
+absorption identity against the MHA oracle over decompressed K/V, brute force),
+fp8 entries (hand-decoded codes, every
 e4m3 code against the library's float8 type, exact products).  No function is "parity unpinned".
 """
 from .bf16 import bf16_bits_to_f64, round_f64_to_bf16
@@ -46,6 +50,7 @@ from .cache_write import cache_write
 from .up_proj import up_project
 from .merge import merge_state
 from .chunked import chunked_prefill_attention
+from .absorbed import absorb_query, absorbed_attention, absorbed_output_to_mha
 from .fp8_cache import (dequant_fp8_entries, e4m3_to_f64, f64_to_bf16_bits, gather_latent_fp8,
                         ue8m0_to_f64)
 
@@ -53,5 +58,5 @@ __all__ = [
     "bf16_bits_to_f64", "round_f64_to_bf16", "allowed_mask", "attend_request",
     "ragged_attention", "gather_latent", "slot_of", "cache_write", "up_project", "merge_state",
     "chunked_prefill_attention", "dequant_fp8_entries", "e4m3_to_f64", "f64_to_bf16_bits",
-    "gather_latent_fp8", "ue8m0_to_f64",
+    "gather_latent_fp8", "ue8m0_to_f64", "absorb_query", "absorbed_attention", "absorbed_output_to_mha",
 ]
