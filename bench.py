@@ -582,8 +582,8 @@ def bench_chunked(args, dev, peaks):
     pipe.check_status()
     stream = torch.cuda.current_stream(dev)
     reps = 5
-    names = ["main_attention", "up_proj_paged", "chunk_attention", "gather", "up_proj", "chunk_attention_unfused",
-             "merge"]
+    names = ["main_attention", "up_proj_paged", "chunk_attention", "gather", "up_proj", "chunk_attention_full_k",
+             "chunk_attention_unfused", "merge"]
     acc = {n: [] for n in names}
     total, total_gathered = [], []
     nC = pipe.cu.shape[0]
@@ -602,7 +602,7 @@ def bench_chunked(args, dev, peaks):
             kc, vc = pipe.k_c[:t], pipe.v_c[:t]
             pipe.decompress(c, cache, table, w, kc, vc)
             evs[i].record(stream)
-            plan.run_merge(q, kc, vc, o, lse)
+            pipe.chunk_attention(c, q, o, lse)
             evs[i + 1].record(stream)
             marks.append((evs[i - 1] if c == 0 else marks[-1][2], evs[i], evs[i + 1]))
             i += 2
@@ -632,13 +632,14 @@ def bench_chunked(args, dev, peaks):
             kc, vc = gpipe.k_c[:t], gpipe.v_c[:t]
             gpipe.decompress(c, cache, table, w, kc, vc)
             evs[i].record(stream)
-            plan.run_merge(q, kc, vc, o, lse)
+            gpipe.chunk_attention(c, q, o, lse)
             evs[i + 1].record(stream)
             i += 2
         torch.cuda.synchronize()
         acc["gather"].append(evs[1].elapsed_time(evs[2]))
         for c in range(nC):
             acc["up_proj"].append(evs[2 + 2 * c].elapsed_time(evs[3 + 2 * c]))
+            acc["chunk_attention_full_k"].append(evs[3 + 2 * c].elapsed_time(evs[4 + 2 * c]))
         total_gathered.append(evs[0].elapsed_time(evs[2 + 2 * nC]))
     gpipe.check_status()
     pipe.latent = gpipe.gather_all(cache, table)
@@ -647,9 +648,9 @@ def bench_chunked(args, dev, peaks):
     o_c = torch.empty_like(o)
     lse_c = torch.empty_like(lse)
     for _ in range(reps):
-        for c, plan in enumerate(pipe.chunks):
-            t = pipe.chunk_tokens[c]
-            kc, vc = pipe.k_c[:t], pipe.v_c[:t]
+        for c, plan in enumerate(gpipe.chunks):
+            t = gpipe.chunk_tokens[c]
+            kc, vc = gpipe.k_c[:t], gpipe.v_c[:t]
             flush.zero_()
             e1, e2, e3 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
             e1.record(stream)
@@ -739,13 +740,19 @@ def bench_chunked(args, dev, peaks):
                            "tflops": round(main_f / med["main_attention"] / 1e9, 2)},
         "chunk_attention": {"ms": round(med["chunk_attention"], 4),
                             "tflops": round(chunk_f / med["chunk_attention"] / 1e9, 2),
-                            "merge": "fused into the attention epilogue (mla_prefill_run_merge)"},
+                            "merge": "fused into the attention epilogue",
+                            "k": "per-head K_nope + one shared rope row per key (mla_prefill_run_shared_rope)"},
+        "chunk_attention_full_k": {"ms": round(med["chunk_attention_full_k"], 4),
+                                   "tflops": round(chunk_f / med["chunk_attention_full_k"] / 1e9, 2),
+                                   "note": "the gathered variant: K [T, H, 192] with the rope in every head "
+                                           "(mla_prefill_run_merge)"},
         "chunk_attention_unfused": {"ms": round(med["chunk_attention_unfused"], 4),
                                     "tflops": round(chunk_f / med["chunk_attention_unfused"] / 1e9, 2),
                                     "plus_merge_ms": round(med["merge"], 4)},
         "up_proj_paged": {"ms": round(med["up_proj_paged"], 4),
                           "tflops": round(upf / med["up_proj_paged"] / 1e9, 2),
-                          "note": "gather + up-projection in one kernel (mla_up_proj_paged), as the pipeline runs"},
+                          "note": "gather + up-projection in one kernel writing K_nope, V and one rope row per "
+                                  "token (mla_up_proj_paged_split), as the pipeline runs"},
         "up_proj": {"ms": round(med["up_proj"], 4), "tflops": round(upf / med["up_proj"] / 1e9, 2),
                     "gbs": round(up_bytes / med["up_proj"] / 1e6, 1),
                     "note": "mla_up_proj on gathered latent rows (the gathered variant)"},

@@ -30,6 +30,8 @@ _SIGNATURES = {
                                   _c_f, _c_int, _c_f, _c_vp]),
     "mla_prefill_run": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
     "mla_prefill_run_merge": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
+    "mla_prefill_run_shared_rope": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp, _c_vp, _c_int,
+                                             _c_vp]),
     "mla_prefill_status": (_c_int, [_c_vp]),
     "mla_plan_destroy": (_c_int, [_c_vp]),
     "mla_plan_query": (_c_int, [_c_vp, _c_int, _i64p]),
@@ -43,6 +45,8 @@ _SIGNATURES = {
     "mla_up_proj": (_c_int, [_c_vp, _c_vp, _c_i64, _c_int, _c_vp, _c_vp, _c_vp, _c_vp]),
     "mla_up_proj_paged": (_c_int, [_c_vp, _c_i64, _c_int, _c_int, _c_vp, _c_int, _c_vp, _c_vp, _c_int, _c_i64,
                                    _c_vp, _c_int, _c_vp, _c_vp, _c_vp, _c_vp]),
+    "mla_up_proj_paged_split": (_c_int, [_c_vp, _c_i64, _c_int, _c_int, _c_vp, _c_int, _c_vp, _c_vp, _c_int,
+                                         _c_i64, _c_vp, _c_int, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
     "mla_merge_state": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_int, _c_int, _c_vp]),
     "mla_prefill_run_noalloc": (_c_int, [_i32p, _i32p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_f, _c_int, _c_f,
                                          _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
@@ -217,6 +221,38 @@ def mla_prefill_run_merge(plan: PrefillPlan, q, k, v, o, lse, stream=None):
     return o, lse
 
 
+def mla_prefill_run_shared_rope(plan: PrefillPlan, q, k_nope, k_rope, v, o=None, lse=None, merge: bool = False,
+                                stream=None):
+    """Run a plan with K = [k_nope (per head) || k_rope (one row per key, shared by all heads)].
+
+    k_nope [T_kv, H, 128]; k_rope: a 2-D [T_kv, 64] view whose rows may be strided (e.g.
+    latent[:, 512:] of a gathered [T_kv, 576] latent).  merge=True merges into (o, lse)."""
+    import torch
+    H = plan.num_heads
+    if tuple(q.shape) != (plan.total_q, H, 192):
+        raise ValueError(f"q must be [{plan.total_q}, {H}, 192], got {tuple(q.shape)}")
+    if tuple(k_nope.shape) != (plan.total_kv, H, 128) or tuple(v.shape) != (plan.total_kv, H, 128):
+        raise ValueError("k_nope/v shapes do not match the plan")
+    if k_rope.dim() != 2 or tuple(k_rope.shape) != (plan.total_kv, 64) or k_rope.stride(1) != 1:
+        raise ValueError("k_rope must be a [T_kv, 64] view with unit column stride")
+    if k_rope.dtype != torch.bfloat16 or not k_rope.is_cuda:
+        raise TypeError("k_rope must be a bf16 CUDA tensor")
+    if merge and (o is None or lse is None):
+        raise ValueError("merge needs the partial state o and lse")
+    if o is None:
+        o = torch.empty((plan.total_q, H, 128), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((plan.total_q, H), dtype=torch.float32, device=q.device)
+    if tuple(o.shape) != (plan.total_q, H, 128) or tuple(lse.shape) != (plan.total_q, H):
+        raise ValueError("o/lse shapes do not match the plan")
+    bf = torch.bfloat16
+    _check(library().mla_prefill_run_shared_rope(plan.handle, _dev(q, bf, "q"), _dev(k_nope, bf, "k_nope"),
+                                                 ctypes.c_void_p(k_rope.data_ptr()), int(k_rope.stride(0)),
+                                                 _dev(v, bf, "v"), _dev(o, bf, "o"), _dev(lse, torch.float32, "lse"),
+                                                 int(bool(merge)), _stream(stream)), "mla_prefill_run_shared_rope")
+    return o, lse
+
+
 def mla_prefill_status(plan: PrefillPlan) -> int:
     """Read-and-clear the plan's device status word; raises on a device-side error."""
     code = library().mla_prefill_status(plan.handle)
@@ -343,6 +379,36 @@ def mla_up_proj_paged(cache, block_table, cu_seq_lens, chunk_starts, total_token
                                        num_heads, _dev(k_out, bf, "k_out"), _dev(v_out, bf, "v_out"),
                                        _dev(status, i32, "status"), _stream(stream)), "mla_up_proj_paged")
     return k_out, v_out
+
+
+def mla_up_proj_paged_split(cache, block_table, cu_seq_lens, chunk_starts, total_tokens: int, w_kvb, num_heads: int,
+                            k_nope_out=None, v_out=None, rope_out=None, status=None, stream=None):
+    """mla_up_proj_paged with K split into K_nope [T, H, 128] and one rope row per token [T, 64]."""
+    import torch
+    nb, bs, e = cache.shape
+    t = int(total_tokens)
+    if e != 576 or tuple(w_kvb.shape) != (512, num_heads * 256):
+        raise ValueError("cache must be [NB, BS, 576] and w_kvb [512, H*256]")
+    batch = block_table.shape[0]
+    if tuple(cu_seq_lens.shape) != (batch + 1,) or tuple(chunk_starts.shape) != (batch,):
+        raise ValueError("cu_seq_lens must be [B+1] and chunk_starts [B] for a block table of B rows")
+    bf, i32 = torch.bfloat16, torch.int32
+    if k_nope_out is None:
+        k_nope_out = torch.empty((t, num_heads, 128), dtype=bf, device=cache.device)
+    if v_out is None:
+        v_out = torch.empty((t, num_heads, 128), dtype=bf, device=cache.device)
+    if rope_out is None:
+        rope_out = torch.empty((t, 64), dtype=bf, device=cache.device)
+    if (tuple(k_nope_out.shape) != (t, num_heads, 128) or tuple(v_out.shape) != (t, num_heads, 128)
+            or tuple(rope_out.shape) != (t, 64)):
+        raise ValueError("k_nope_out/v_out/rope_out shapes do not match total_tokens and num_heads")
+    _check(library().mla_up_proj_paged_split(_dev(cache, bf, "cache"), nb, bs, e, _dev(block_table, i32, "block_table"),
+                                             block_table.shape[1], _dev(cu_seq_lens, i32, "cu_seq_lens"),
+                                             _dev(chunk_starts, i32, "chunk_starts"), batch, t,
+                                             _dev(w_kvb, bf, "w_kvb"), num_heads, _dev(k_nope_out, bf, "k_nope_out"),
+                                             _dev(v_out, bf, "v_out"), _dev(rope_out, bf, "rope_out"),
+                                             _dev(status, i32, "status"), _stream(stream)), "mla_up_proj_paged_split")
+    return k_nope_out, v_out, rope_out
 
 
 def mla_merge_state(o_a, lse_a, o_b, lse_b, o_out=None, lse_out=None, stream=None):

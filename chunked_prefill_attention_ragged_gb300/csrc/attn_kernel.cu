@@ -127,7 +127,7 @@ __device__ __forceinline__ Unit load_unit(const Unit* units, int i) {
 // stage: warp 0 loads Q (once per unit) and K tiles, warp 2 loads V tiles.  A K stage
 // frees when its S = Q K^T is done, a V stage when its P V is done.
 __device__ void run_producer_qk(const Ctx& c, const PrefillParams& p, const CUtensorMap* tq,
-                                const CUtensorMap* tk, int ubeg, int uend) {
+                                const CUtensorMap* tk, const CUtensorMap* tr, int ubeg, int uend) {
   int q_g = 0, k_g = 0;   // loads issued so far (Q tiles, K tiles)
   bool ok = true;
   for (int ui = ubeg; ui < uend && ok; ++ui) {
@@ -145,8 +145,15 @@ __device__ void run_producer_qk(const Ctx& c, const PrefillParams& p, const CUte
       const uint32_t use = k_g / NSTAGE;
       if (use > 0 && !c.wait(KE + s, (use - 1) & 1)) { ok = false; break; }
       mbar_arrive_expect_tx(c.bar(KF + s), K_PANELS * PANEL);
-      for (int i = 0; i < K_PANELS; ++i)
-        tma_load_3d(c.sbase + OFF_K + (s * K_PANELS + i) * PANEL, tk, c.bar(KF + s), i * 64, u.head, row);
+      // Panels 0-1 are K's NoPE columns; panel 2 its RoPE columns, which with a shared
+      // rope come from the one [tokens, 64] rope tensor that every head uses.
+      for (int i = 0; i < K_PANELS; ++i) {
+        const uint32_t dst = c.sbase + OFF_K + (s * K_PANELS + i) * PANEL;
+        if (p.shared_rope && i == K_PANELS - 1)
+          tma_load_2d(dst, tr, c.bar(KF + s), 0, row);
+        else
+          tma_load_3d(dst, tk, c.bar(KF + s), i * 64, u.head, row);
+      }
       ++k_g;
     }
   }
@@ -585,7 +592,8 @@ __device__ void run_epilogue(const Ctx& c, const PrefillParams& p, uint32_t tmem
 template <bool kMerge>
 __global__ void __launch_bounds__(NTHREADS, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
+               const PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -609,6 +617,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
+    if (p.shared_rope) tma_prefetch_desc(&tm_r);
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
@@ -624,7 +633,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   if (warp < 4) {
     setmaxnreg_dec<RegSplit<kMerge>::ctrl>();
     if (lane == 0) {
-      if (warp == 0) run_producer_qk(c, p, &tm_q, &tm_k, ubeg, uend);
+      if (warp == 0) run_producer_qk(c, p, &tm_q, &tm_k, &tm_r, ubeg, uend);
       else if (warp == 1) run_mma_qk(c, p, tmem, ubeg, uend);
       else if (warp == 2) run_producer_v(c, p, &tm_v, ubeg, uend);
       else run_mma_pv(c, p, tmem, ubeg, uend);
@@ -651,7 +660,8 @@ int prefill_smem_bytes() { return SMEM_BYTES; }
 
 template <bool kMerge>
 static cudaError_t launch_prefill_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                    const PrefillParams& p, int num_ctas, cudaStream_t stream) {
+                                    const CUtensorMap& tr, const PrefillParams& p, int num_ctas,
+                                    cudaStream_t stream) {
   static PerDeviceOnce configured;
   cudaError_t e = configured.run([] {
     cudaError_t r = cudaFuncSetAttribute(prefill_kernel<kMerge>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -665,14 +675,14 @@ static cudaError_t launch_prefill_t(const CUtensorMap& tq, const CUtensorMap& tk
     return attr.numRegs == LAUNCH_REGS ? cudaSuccess : cudaErrorInvalidConfiguration;
   });
   if (e != cudaSuccess) return e;
-  prefill_kernel<kMerge><<<num_ctas, NTHREADS, SMEM_BYTES, stream>>>(tq, tk, tv, p);
+  prefill_kernel<kMerge><<<num_ctas, NTHREADS, SMEM_BYTES, stream>>>(tq, tk, tv, tr, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const PrefillParams& p, int num_ctas, cudaStream_t stream) {
-  return p.merge ? launch_prefill_t<true>(tq, tk, tv, p, num_ctas, stream)
-                 : launch_prefill_t<false>(tq, tk, tv, p, num_ctas, stream);
+                           const CUtensorMap& tr, const PrefillParams& p, int num_ctas, cudaStream_t stream) {
+  return p.merge ? launch_prefill_t<true>(tq, tk, tv, tr, p, num_ctas, stream)
+                 : launch_prefill_t<false>(tq, tk, tv, tr, p, num_ctas, stream);
 }
 
 }  // namespace mla

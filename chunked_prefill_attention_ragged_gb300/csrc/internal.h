@@ -31,6 +31,7 @@ struct PrefillParams {
   float cap_ex2_scale;        // 2 * log2(e) * sm_scale / logits_soft_cap: e^(2y) = 2^(x * this)
   uint64_t wait_limit_ns;     // a pipeline wait gives up after this long (default 2 s)
   int force_timeout;          // test mode: one wait that nothing satisfies (see below)
+  int shared_rope;            // K's RoPE columns come from one [kv rows, 64] tensor (map tm_r)
 };
 
 // Time-out test mode.  When the environment variable MLA_TEST_FORCE_TIMEOUT_NS holds a
@@ -43,8 +44,9 @@ uint64_t forced_timeout_ns();
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // the normal limit of a pipeline wait
 
 int prefill_smem_bytes();
+// tr: the shared RoPE tensor's map when p.shared_rope is set (any valid map otherwise).
 cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const PrefillParams& p, int num_ctas, cudaStream_t stream);
+                           const CUtensorMap& tr, const PrefillParams& p, int num_ctas, cudaStream_t stream);
 
 // ---- tensor maps (tma.cpp) ---------------------------------------------------
 // bf16 tensor of rank 2 or 3 (dims innermost first, strides in bytes for dims 1..),
@@ -74,8 +76,8 @@ cudaError_t launch_up_proj(const CUtensorMap& ta, const CUtensorMap& tb, const v
 cudaError_t launch_up_proj_paged(const CUtensorMap& ta, const CUtensorMap& tb, const void* cache, int64_t num_blocks,
                                  int block_size, const int32_t* block_table, int max_blocks_per_req,
                                  const int32_t* cu_seq_lens, const int32_t* chunk_starts, int batch,
-                                 int64_t total_tokens, int num_heads, void* k_out, void* v_out, int32_t* status,
-                                 cudaStream_t stream);
+                                 int64_t total_tokens, int num_heads, void* k_out, void* v_out, void* rope_out,
+                                 int32_t* status, cudaStream_t stream);
 
 cudaError_t launch_merge(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,
                          void* o_out, float* lse_out, int64_t rows, int num_heads, int head_dim,

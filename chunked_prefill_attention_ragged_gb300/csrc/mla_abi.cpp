@@ -161,14 +161,19 @@ int mla_prefill_plan(mla_plan_t* out, const int32_t* qo_indptr, const int32_t* k
   return MLA_OK;
 }
 
-static int prefill_run_impl(mla_plan_t p, const void* q, const void* k, const void* v, void* o, float* lse,
-                            int merge, void* stream) {
+// k_rope == nullptr: K is [kv rows, H, 192].  Otherwise K is given as k = K_nope [kv rows,
+// H, 128] and k_rope = the one RoPE row per key, rope_stride elements apart, shared by all
+// heads.
+static int prefill_run_impl(mla_plan_t p, const void* q, const void* k, const void* k_rope, int64_t rope_stride,
+                            const void* v, void* o, float* lse, int merge, void* stream) {
   if (!p) return MLA_ERR_INVALID_ARG;
   if (merge && !lse) return MLA_ERR_INVALID_ARG;
   if (p->plan.units.empty()) return MLA_OK;   // no query rows
   if (!q || !o || !aligned16(q) || !aligned16(o) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
     return MLA_ERR_INVALID_ARG;
   if (p->total_kv > 0 && (!k || !v || !aligned16(k) || !aligned16(v))) return MLA_ERR_INVALID_ARG;
+  const bool shared_rope = k_rope != nullptr;
+  if (shared_rope && (!aligned16(k_rope) || rope_stride < 64 || rope_stride % 8 != 0)) return MLA_ERR_INVALID_ARG;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != p->device) return MLA_ERR_INVALID_ARG;
 
@@ -177,7 +182,7 @@ static int prefill_run_impl(mla_plan_t p, const void* q, const void* k, const vo
   const void* vb = p->total_kv > 0 ? v : q;
   const uint64_t H = (uint64_t)p->num_heads;
   const uint64_t kv_rows = p->total_kv > 0 ? (uint64_t)p->total_kv : 1;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, tr;
   const uint32_t box[3] = {64, 1, 128};
   {
     const uint64_t dims[3] = {192, H, (uint64_t)p->total_q};
@@ -185,9 +190,18 @@ static int prefill_run_impl(mla_plan_t p, const void* q, const void* k, const vo
     if (make_tensor_map_bf16(&tq, q, 3, dims, strides, box) != MLA_OK) return MLA_ERR_CUDA;
   }
   {
-    const uint64_t dims[3] = {192, H, kv_rows};
-    const uint64_t strides[2] = {192 * 2, H * 192 * 2};
+    const uint64_t kd = shared_rope ? 128 : 192;
+    const uint64_t dims[3] = {kd, H, kv_rows};
+    const uint64_t strides[2] = {kd * 2, H * kd * 2};
     if (make_tensor_map_bf16(&tk, kb, 3, dims, strides, box) != MLA_OK) return MLA_ERR_CUDA;
+  }
+  if (shared_rope && p->total_kv > 0) {
+    const uint64_t dims[2] = {64, kv_rows};
+    const uint64_t strides[1] = {(uint64_t)rope_stride * 2};
+    const uint32_t rbox[2] = {64, 128};
+    if (make_tensor_map_bf16(&tr, k_rope, 2, dims, strides, rbox) != MLA_OK) return MLA_ERR_CUDA;
+  } else {
+    tr = tk;
   }
   {
     const uint64_t dims[3] = {128, H, kv_rows};
@@ -213,8 +227,9 @@ static int prefill_run_impl(mla_plan_t p, const void* q, const void* k, const vo
   prm.cap_ex2_scale = 2.f * LOG2E * prm.x_to_cap;
   prm.force_timeout = p->forced_timeout_ns != 0;
   prm.wait_limit_ns = prm.force_timeout ? p->forced_timeout_ns : kWaitLimitNs;
+  prm.shared_rope = shared_rope && p->total_kv > 0;
   const cudaStream_t s = as_stream(stream);
-  if (launch_prefill(tq, tk, tv, prm, p->num_ctas, s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_prefill(tq, tk, tv, tr, prm, p->num_ctas, s) != cudaSuccess) return MLA_ERR_CUDA;
   // Remember the last use for mla_plan_destroy.  A run captured into a graph is not
   // recorded: the plan must then outlive every launch of that graph.
   if (!stream_capturing(s) && cudaEventRecord(p->last_use, s) != cudaSuccess) return MLA_ERR_CUDA;
@@ -223,12 +238,18 @@ static int prefill_run_impl(mla_plan_t p, const void* q, const void* k, const vo
 
 int mla_prefill_run(mla_plan_t p, const void* q, const void* k, const void* v, void* o, float* lse,
                     void* stream) {
-  return prefill_run_impl(p, q, k, v, o, lse, 0, stream);
+  return prefill_run_impl(p, q, k, nullptr, 0, v, o, lse, 0, stream);
 }
 
 int mla_prefill_run_merge(mla_plan_t p, const void* q, const void* k, const void* v, void* o, float* lse,
                           void* stream) {
-  return prefill_run_impl(p, q, k, v, o, lse, 1, stream);
+  return prefill_run_impl(p, q, k, nullptr, 0, v, o, lse, 1, stream);
+}
+
+int mla_prefill_run_shared_rope(mla_plan_t p, const void* q, const void* k_nope, const void* k_rope,
+                                int64_t rope_stride, const void* v, void* o, float* lse, int merge, void* stream) {
+  if (!k_rope && p && p->total_kv > 0) return MLA_ERR_INVALID_ARG;
+  return prefill_run_impl(p, q, k_nope, k_rope, rope_stride, v, o, lse, merge != 0, stream);
 }
 
 int mla_prefill_status(mla_plan_t p) {
@@ -358,10 +379,11 @@ int mla_up_proj(const void* latent, const void* w_kvb, int64_t num_tokens, int n
              : MLA_ERR_CUDA;
 }
 
-int mla_up_proj_paged(const void* cache, int64_t num_blocks, int block_size, int entry_dim,
-                      const int32_t* block_table, int max_blocks_per_req, const int32_t* cu_seq_lens,
-                      const int32_t* chunk_starts, int batch, int64_t total_tokens, const void* w_kvb, int num_heads,
-                      void* k_out, void* v_out, int32_t* status, void* stream) {
+static int up_proj_paged_impl(const void* cache, int64_t num_blocks, int block_size, int entry_dim,
+                              const int32_t* block_table, int max_blocks_per_req, const int32_t* cu_seq_lens,
+                              const int32_t* chunk_starts, int batch, int64_t total_tokens, const void* w_kvb,
+                              int num_heads, void* k_out, void* v_out, void* rope_out, int32_t* status,
+                              void* stream) {
   if (total_tokens < 0 || batch < 0 || num_blocks < 0 || block_size < 1 || max_blocks_per_req < 0 ||
       num_heads < 1)
     return MLA_ERR_INVALID_ARG;
@@ -389,11 +411,32 @@ int mla_up_proj_paged(const void* cache, int64_t num_blocks, int block_size, int
     const uint32_t box[2] = {64, 64};
     if (make_tensor_map_bf16(&tb, w_kvb, 2, dims, strides, box) != MLA_OK) return MLA_ERR_CUDA;
   }
+  if (rope_out && !aligned16(rope_out)) return MLA_ERR_INVALID_ARG;
   return launch_up_proj_paged(ta, tb, cache, num_blocks, block_size, block_table, max_blocks_per_req, cu_seq_lens,
-                              chunk_starts, batch, total_tokens, num_heads, k_out, v_out, status,
+                              chunk_starts, batch, total_tokens, num_heads, k_out, v_out, rope_out, status,
                               as_stream(stream)) == cudaSuccess
              ? MLA_OK
              : MLA_ERR_CUDA;
+}
+
+int mla_up_proj_paged(const void* cache, int64_t num_blocks, int block_size, int entry_dim,
+                      const int32_t* block_table, int max_blocks_per_req, const int32_t* cu_seq_lens,
+                      const int32_t* chunk_starts, int batch, int64_t total_tokens, const void* w_kvb, int num_heads,
+                      void* k_out, void* v_out, int32_t* status, void* stream) {
+  return up_proj_paged_impl(cache, num_blocks, block_size, entry_dim, block_table, max_blocks_per_req, cu_seq_lens,
+                            chunk_starts, batch, total_tokens, w_kvb, num_heads, k_out, v_out, nullptr, status,
+                            stream);
+}
+
+int mla_up_proj_paged_split(const void* cache, int64_t num_blocks, int block_size, int entry_dim,
+                            const int32_t* block_table, int max_blocks_per_req, const int32_t* cu_seq_lens,
+                            const int32_t* chunk_starts, int batch, int64_t total_tokens, const void* w_kvb,
+                            int num_heads, void* k_nope_out, void* v_out, void* rope_out, int32_t* status,
+                            void* stream) {
+  if (!rope_out && total_tokens > 0) return MLA_ERR_INVALID_ARG;
+  return up_proj_paged_impl(cache, num_blocks, block_size, entry_dim, block_table, max_blocks_per_req, cu_seq_lens,
+                            chunk_starts, batch, total_tokens, w_kvb, num_heads, k_nope_out, v_out, rope_out, status,
+                            stream);
 }
 
 int mla_merge_state(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b, void* o_out,

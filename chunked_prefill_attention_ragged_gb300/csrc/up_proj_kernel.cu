@@ -75,6 +75,10 @@ struct UpParams {
   int num_heads;
   int num_tiles;
   int out_align32;   // k and v 32-byte aligned: 32-byte stores
+  // split form: k holds K_nope [T, H, 128] only and rope_out [T, 64] the one RoPE row per
+  // token that every head's K shares (written once, by the tile of head 0)
+  __nv_bfloat16* rope_out;
+  int split_rope;
   // paged form: token row t of the output is the cache row of the chunk's row t
   RowMap rows;
   int32_t oob_row;   // a row coordinate past the cache: the TMA fills it with zeros
@@ -253,7 +257,7 @@ up_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
       }
       if (!__all_sync(0xffffffffu, c.wait(AFULL + a, (acc >> 1) & 1))) break;
       tc_fence_after();
-      const int64_t kr = (t * H + h) * 192, vr = (t * H + h) * 128;
+      const int64_t kr = (t * H + h) * (p.split_rope ? 128 : 192), vr = (t * H + h) * 128;
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t r[64];
@@ -275,8 +279,8 @@ up_proj_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__
       }
       tc_fence_before();
       mbar_arrive(c.bar(AEMPTY + a));
-      if (live) {
-        uint4* dst = reinterpret_cast<uint4*>(p.k + kr + 128);
+      if (live && (!p.split_rope || h == 0)) {
+        uint4* dst = reinterpret_cast<uint4*>(p.split_rope ? p.rope_out + t * 64 : p.k + kr + 128);
 #pragma unroll
         for (int i = 0; i < 8; ++i) dst[i] = rope[i];
       }
@@ -334,9 +338,12 @@ cudaError_t launch_up_proj(const CUtensorMap& ta, const CUtensorMap& tb, const v
 cudaError_t launch_up_proj_paged(const CUtensorMap& ta, const CUtensorMap& tb, const void* cache, int64_t num_blocks,
                                  int block_size, const int32_t* block_table, int max_blocks_per_req,
                                  const int32_t* cu_seq_lens, const int32_t* chunk_starts, int batch,
-                                 int64_t total_tokens, int num_heads, void* k_out, void* v_out, int32_t* status,
-                                 cudaStream_t stream) {
+                                 int64_t total_tokens, int num_heads, void* k_out, void* v_out, void* rope_out,
+                                 int32_t* status, cudaStream_t stream) {
   UpParams p = up_params(cache, total_tokens, num_heads, k_out, v_out, status);
+  p.rope_out = static_cast<__nv_bfloat16*>(rope_out);
+  p.split_rope = rope_out != nullptr;
+  if (p.split_rope) p.out_align32 = p.out_align32 && (reinterpret_cast<uintptr_t>(rope_out) & 31u) == 0;
   p.rows = RowMap{cu_seq_lens, chunk_starts, block_table, batch, max_blocks_per_req, block_size, num_blocks};
   p.oob_row = (int32_t)(num_blocks * block_size);
   return launch_up_proj_t<true>(ta, tb, p, stream);

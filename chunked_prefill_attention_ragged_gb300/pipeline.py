@@ -10,9 +10,11 @@ prefix lives in the paged cache as 512 latent + 64 rope per token and is
 decompressed before attention.
 
 Per run: new-token attention -> for every chunk: the chunk's K/V decompressed
-straight out of the paged cache (mla_up_proj_paged: gather and up-projection in
-one kernel, no gathered latent buffer) -> non-causal attention merged into the
-running (O, LSE) by the attention kernel's epilogue (mla_prefill_run_merge).
+straight out of the paged cache (mla_up_proj_paged_split: gather and
+up-projection in one kernel, no gathered latent buffer, K as per-head K_nope
+plus one rope row per token, since every head's K carries the same rope) ->
+non-causal attention merged into the running (O, LSE) by the attention
+kernel's epilogue (mla_prefill_run_shared_rope with merge).
 Variants, the same result up to rounding: with paged_up_proj=False one gather
 of every chunk's latent rows (one launch, large enough to run near HBM
 bandwidth) feeds mla_up_proj; with fuse_merge=False the attention writes its
@@ -28,8 +30,8 @@ from __future__ import annotations
 
 import numpy as np
 
-from ._binding import (mla_gather_latent, mla_gather_latent_fp8, mla_merge_state, mla_prefill_plan, mla_up_proj,
-                       mla_up_proj_paged)
+from ._binding import (mla_gather_latent, mla_gather_latent_fp8, mla_merge_state, mla_prefill_plan,
+                       mla_prefill_run_shared_rope, mla_up_proj, mla_up_proj_paged, mla_up_proj_paged_split)
 
 
 class ChunkedPrefill:
@@ -81,7 +83,10 @@ class ChunkedPrefill:
         self.paged_up_proj = bool(paged_up_proj) and not self.cache_fp8
         self.latent = None if self.paged_up_proj else torch.empty((max(self.total_prefix, 1), 576), dtype=bf,
                                                                    device=device)
-        self.k_c = torch.empty((max(t_max, 1), h, 192), dtype=bf, device=device)
+        # K of a chunk: [T, H, 192], or with the shared rope K_nope [T, H, 128] + rope [T, 64]
+        self.shared_rope = self.paged_up_proj
+        self.k_c = torch.empty((max(t_max, 1), h, 128 if self.shared_rope else 192), dtype=bf, device=device)
+        self.rope_c = torch.empty((max(t_max, 1), 64), dtype=bf, device=device) if self.shared_rope else None
         self.v_c = torch.empty((max(t_max, 1), h, 128), dtype=bf, device=device)
         self.fuse_merge = bool(fuse_merge)
         if self.fuse_merge:
@@ -130,18 +135,34 @@ class ChunkedPrefill:
                 continue
             kc, vc = self.k_c[:t], self.v_c[:t]
             self.decompress(c, cache, block_table, w_kvb, kc, vc, stream)
-            if self.fuse_merge:
-                plan.run_merge(q, kc, vc, o, lse, stream)
-            else:
-                oc, lc = self.o_c[:self.total_q], self.lse_c[:self.total_q]
-                plan.run(q, kc, vc, oc, lc, True, stream)
-                mla_merge_state(o, lse, oc, lc, o, lse, stream)
+            self.chunk_attention(c, q, o, lse, stream)
         return o, lse
 
+    def chunk_attention(self, c, q, o, lse, stream=None):
+        """Chunk c's non-causal attention over its decompressed K/V, merged into (o, lse)."""
+        t, plan = self.chunk_tokens[c], self.chunks[c]
+        kc, vc = self.k_c[:t], self.v_c[:t]
+        if self.fuse_merge:
+            if self.shared_rope:
+                mla_prefill_run_shared_rope(plan, q, kc, self.rope_c[:t], vc, o, lse, True, stream)
+            else:
+                plan.run_merge(q, kc, vc, o, lse, stream)
+        else:
+            oc, lc = self.o_c[:self.total_q], self.lse_c[:self.total_q]
+            if self.shared_rope:
+                mla_prefill_run_shared_rope(plan, q, kc, self.rope_c[:t], vc, oc, lc, False, stream)
+            else:
+                plan.run(q, kc, vc, oc, lc, True, stream)
+            mla_merge_state(o, lse, oc, lc, o, lse, stream)
+
     def decompress(self, c, cache, block_table, w_kvb, kc, vc, stream=None):
-        """Chunk c's K [T, H, 192] and V [T, H, 128] into kc, vc."""
+        """Chunk c's K and V [T, H, 128] into kc, vc (K [T, H, 192], or K_nope [T, H, 128] with
+        the rope rows in self.rope_c when the rope is shared)."""
         t = self.chunk_tokens[c]
-        if self.paged_up_proj:
+        if self.shared_rope:
+            mla_up_proj_paged_split(cache, block_table, self.cu_dev[c], self.starts_dev[c], t, w_kvb, self.num_heads,
+                                    kc, vc, self.rope_c[:t], self.status, stream)
+        elif self.paged_up_proj:
             mla_up_proj_paged(cache, block_table, self.cu_dev[c], self.starts_dev[c], t, w_kvb, self.num_heads, kc, vc,
                               self.status, stream)
         else:

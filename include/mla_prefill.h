@@ -140,6 +140,27 @@ MLA_API int mla_prefill_run_merge(mla_plan_t plan, const void* q, const void* k,
                                   float* lse, void* stream);
 
 /*
+ * Run a planned problem with K given in two parts: the per-head NoPE columns and ONE RoPE
+ * row per key shared by every head.  [sglang]: the cache keeps a single 64-dim rope per
+ * token, so after decompression K = [K_nope(h) || rope] repeats the same 64 values in
+ * every head; [vLLM-FI]: the latent cache has one KV head.  Reading the rope once per key
+ * instead of once per (key, head) saves the decompression 20 % of its output and the
+ * attention a third of its K bytes.  Same result, bit for bit, as mla_prefill_run /
+ * mla_prefill_run_merge on the concatenated K.
+ *   k_nope      : bf16 [kv_indptr[batch], num_heads, 128]
+ *   k_rope      : bf16, row t (key t) at k_rope + t * rope_stride, 64 values; rope_stride
+ *                 (elements) >= 64 and a multiple of 8, k_rope 16-byte aligned.  E.g. the
+ *                 rope columns of a gathered latent [T, 576]: k_rope = latent + 512,
+ *                 rope_stride = 576.
+ *   merge       : 0 = write O/LSE (as mla_prefill_run), 1 = merge into o/lse (as
+ *                 mla_prefill_run_merge; lse required)
+ * Other arguments as for mla_prefill_run.
+ */
+MLA_API int mla_prefill_run_shared_rope(mla_plan_t plan, const void* q, const void* k_nope, const void* k_rope,
+                                        int64_t rope_stride, const void* v, void* o, float* lse, int merge,
+                                        void* stream);
+
+/*
  * Read and clear the plan's device status word (a blocking device-to-host
  * copy; call after the run's stream has completed).  Returns MLA_OK,
  * MLA_ERR_DEVICE_TIMEOUT or MLA_ERR_CUDA.
@@ -284,6 +305,20 @@ MLA_API int mla_up_proj_paged(const void* cache, int64_t num_blocks, int block_s
                               const int32_t* block_table, int max_blocks_per_req, const int32_t* cu_seq_lens,
                               const int32_t* chunk_starts, int batch, int64_t total_tokens, const void* w_kvb,
                               int num_heads, void* k_out, void* v_out, int32_t* status, void* stream);
+
+/*
+ * mla_up_proj_paged with K in the two parts mla_prefill_run_shared_rope takes:
+ *   k_nope_out : bf16 [total_tokens, num_heads, 128] = the K_nope of mla_up_proj_paged's K
+ *   rope_out   : bf16 [total_tokens, 64] = each row's rope (K's last 64 columns, the same in
+ *                every head), written once per token; 16-byte aligned, required
+ *   v_out      : as for mla_up_proj_paged
+ * Bit-identical to the corresponding parts of mla_up_proj_paged's output.
+ */
+MLA_API int mla_up_proj_paged_split(const void* cache, int64_t num_blocks, int block_size, int entry_dim,
+                                    const int32_t* block_table, int max_blocks_per_req, const int32_t* cu_seq_lens,
+                                    const int32_t* chunk_starts, int batch, int64_t total_tokens, const void* w_kvb,
+                                    int num_heads, void* k_nope_out, void* v_out, void* rope_out, int32_t* status,
+                                    void* stream);
 
 /* ======================================================================
  * LSE merge of two partial attention states.  [vLLM-FI]

@@ -177,3 +177,48 @@ def test_workload3_long_sampled():
     o_ref, lse_ref = oracle_parallel(b, rows=rows)
     idx = torch.from_numpy(np.concatenate([b.qo_indptr[r] + rows[r] for r in range(b.batch)])).cuda()
     check_attention(f64_of_bf16(o[idx]), lse[idx].double().cpu().numpy(), o_ref, lse_ref, "workload3")
+
+
+@pytest.mark.parametrize("merge", [False, True])
+@pytest.mark.parametrize("strided", [False, True])
+def test_shared_rope_equals_full_k(merge, strided):
+    """K given as per-head K_nope plus one rope row per key (the same in every head) gives
+    bit for bit what the concatenated K [T, H, 192] gives; the rope may be a strided view
+    (the rope columns of a [T, 576] latent)."""
+    import chunked_prefill_attention_ragged_gb300 as mla
+    b = wl.random_ragged(91, [300, 77, 1], [700, 129, 5], 4, causal=False)
+    rng = np.random.default_rng(92)
+    t = b.k.shape[0]
+    rope = wl.to_bf16_bits(rng.standard_normal((t, 64)).astype(np.float32))
+    b.k[:, :, 128:] = rope[:, None, :]                      # the full K carries the rope in every head
+    plan = mla.mla_prefill_plan(b.qo_indptr, b.kv_indptr, 4, causal=False, sm_scale=b.sm_scale)
+    q, k, v = to_dev_bf16(b.q), to_dev_bf16(b.k), to_dev_bf16(b.v)
+    k_nope = k[:, :, :128].contiguous()
+    if strided:
+        lat = torch.zeros(t, 576, dtype=torch.bfloat16, device="cuda")
+        lat[:, 512:] = to_dev_bf16(rope)
+        k_rope = lat[:, 512:]
+    else:
+        k_rope = to_dev_bf16(rope)
+    rows = b.q.shape[0]
+    o0 = torch.randn(rows, 4, 128, device="cuda").to(torch.bfloat16)
+    l0 = torch.randn(rows, 4, device="cuda")
+    if merge:
+        o_ref, l_ref = plan.run_merge(q, k, v, o0.clone(), l0.clone())
+        g_o, g_l = Guarded((rows, 4, 128), torch.bfloat16), Guarded((rows, 4), torch.float32)
+        g_o.tensor.copy_(o0)
+        g_l.tensor.copy_(l0)
+        o, l = mla.mla_prefill_run_shared_rope(plan, q, k_nope, k_rope, v, g_o.tensor, g_l.tensor, merge=True)
+    else:
+        o_ref, l_ref = plan.run(q, k, v)
+        g_o, g_l = Guarded((rows, 4, 128), torch.bfloat16), Guarded((rows, 4), torch.float32)
+        o, l = mla.mla_prefill_run_shared_rope(plan, q, k_nope, k_rope, v, g_o.tensor, g_l.tensor)
+    torch.cuda.synchronize()
+    assert plan.status() == 0
+    g_o.check("shared-rope O")
+    g_l.check("shared-rope LSE")
+    assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16))
+    assert torch.equal(l, l_ref)
+    if not merge:
+        o_or, l_or = oracle(b)
+        check_attention(f64_of_bf16(o), l.double().cpu().numpy(), o_or, l_or, "shared rope")

@@ -399,3 +399,27 @@ def test_gather_fp8_bad_block_flags_and_zeroes():
     good_table = np.array([[0, 1], [2, 3]], dtype=np.int32)
     keep = np.setdiff1d(np.arange(140), bad)
     np.testing.assert_array_equal(got[keep], gather_latent_fp8(cache, good_table, cu, st)[keep])
+
+
+def test_up_proj_paged_split_matches_paged():
+    """The split form writes K_nope, V and one rope row per token: bit-identical to the
+    corresponding parts of the paged up-projection's K [T, H, 192] and V."""
+    mla = _mla()
+    cb = wl.random_chunked_prefix(93, [1, 1, 1], [700, 129, 1000], 3, num_blocks=40, block_size=64,
+                                  chunk_tokens=512)
+    cache, table, w = to_dev_bf16(cb.cache), to_dev(cb.block_table), to_dev_bf16(cb.w_kvb)
+    for c in range(cb.layout.num_chunks):
+        cu, st = to_dev(cb.layout.cu_seq_lens[c]), to_dev(cb.layout.chunk_starts[c])
+        t = int(cb.layout.cu_seq_lens[c][-1])
+        k, v = mla.mla_up_proj_paged(cache, table, cu, st, t, w, 3)
+        g_k, g_v, g_r = (Guarded((t, 3, 128), torch.bfloat16), Guarded((t, 3, 128), torch.bfloat16),
+                         Guarded((t, 64), torch.bfloat16))
+        kn, v2, rope = mla.mla_up_proj_paged_split(cache, table, cu, st, t, w, 3, g_k.tensor, g_v.tensor, g_r.tensor)
+        torch.cuda.synchronize()
+        for g, what in ((g_k, "K_nope"), (g_v, "V"), (g_r, "rope")):
+            g.check(what)
+        assert torch.equal(kn.view(torch.int16), k[:, :, :128].contiguous().view(torch.int16))
+        assert torch.equal(v2.view(torch.int16), v.view(torch.int16))
+        assert torch.equal(rope.view(torch.int16), k[:, 0, 128:].contiguous().view(torch.int16))
+        lat = gather_latent(cb.cache, cb.block_table, cb.layout.cu_seq_lens[c], cb.layout.chunk_starts[c])
+        np.testing.assert_array_equal(bits_of(rope), lat[:, 512:])
