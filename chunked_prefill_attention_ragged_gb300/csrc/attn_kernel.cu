@@ -68,9 +68,10 @@ enum Bar {
 };
 // Parity waits: a wait for phase f of a barrier is exact only while phase f - 1 has
 // completed and phase f + 1 cannot have.  O-done is split by tile parity so that the
-// softmax (which skips each unit's last product) and the epilogue (which waits only for
-// it) both meet that: products complete in order, P(g - 3) V has completed whenever S(g)
-// exists, and P(g + 1) V needs a P (or the epilogue's release of O) not yet given.
+// softmax (which waits for product g - 1 only when tile g rescales O) and the epilogue
+// (which waits for a unit's last two products) both meet that: products complete in
+// order, P(g - 3) V has completed whenever S(g) exists, and P(g + 1) V needs a P (or the
+// epilogue's release of O) not yet given.
 // Exchange area: row max per (tile parity, half) and, per unit parity, both halves'
 // row sums and the row max, 10 x 128 floats.
 constexpr int OFF_XCHG = OFF_BAR + NBAR * 8;
@@ -368,16 +369,18 @@ __device__ void run_softmax(const Ctx& c, const PrefillParams& p, uint32_t tmem,
       const float sum = s01.x + s01.y;
       tmem_st32_sync(lane_addr + TM_S(b) + half * 32, pr);
       float alpha = 1.f;
-      if (j > 0) {
+      // tcgen05.ld/st are warp-collective (.sync.aligned): the whole warp rescales its 32
+      // rows together, rows that keep their max with alpha = 1.  A warp none of whose rows
+      // rescale does not touch O and need not wait for the previous product: products
+      // accumulate in issue order, so P_j V_j may queue behind P_{j-1} V_{j-1}.
+      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
         // O must hold P_{j-1} V_{j-1} before it may be rescaled (tiles and products are
         // counted alike: that product is tile sg - 1).
         const int pg = sg - 1;
         if (!__all_sync(0xffffffffu, c.wait(OD + (pg & 1), (pg >> 1) & 1))) { ok = false; break; }
         tc_fence_after();
         if (rescale) alpha = ex2_approx(m_used - m_new);
-        // tcgen05.ld/st are warp-collective (.sync.aligned): the whole warp rescales
-        // its 32 rows together, rows that keep their max with alpha = 1.
-        if (__any_sync(0xffffffffu, rescale)) {
+        {
           float ov[64];
           tmem_ld64_sync(lane_addr + TM_O + half * 64, reinterpret_cast<uint32_t*>(ov));
           const float2 a2 = make_float2(alpha, alpha);
@@ -517,9 +520,13 @@ __device__ void run_epilogue(const Ctx& c, const PrefillParams& p, uint32_t tmem
     const float l_row = xlm[(slot * 3 + 0) * 128 + row] + xlm[(slot * 3 + 1) * 128 + row];
     const float m_row = xlm[(slot * 3 + 2) * 128 + row];
     mbar_arrive(c.bar(LFR + slot));
-    // The unit's last product.  The one before it on the same barrier (tile gl - 2) has
-    // completed: the softmax waited for tile gl - 1 (n > 1) or this warp did (n = 1).
+    // The unit's last product.  A parity wait on it is exact only once the product before
+    // it on the same barrier (tile gl - 2) has completed: for n = 1 this warp waited for
+    // tile gl - 1 (the previous unit's last product); for n > 1 it waits for tile gl - 1
+    // first (whose own predecessor, tile gl - 3, has completed: S of tile gl exists).
+    // Products complete in order, so gl - 1 done means gl - 2 done.
     const int gl = g + n - 1;
+    if (n > 1 && !__all_sync(0xffffffffu, c.wait(OD + ((gl - 1) & 1), ((gl - 1) >> 1) & 1))) break;
     if (!__all_sync(0xffffffffu, c.wait(OD + (gl & 1), (gl >> 1) & 1))) break;
     tc_fence_after();
     const bool live = row < u.q_rows;
