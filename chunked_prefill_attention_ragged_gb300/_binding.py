@@ -235,10 +235,10 @@ def mla_prefill_run_shared_rope(plan: PrefillPlan, q, k_nope, k_rope, v, o=None,
         raise ValueError("k_nope/v shapes do not match the plan")
     if k_rope.dim() != 2 or tuple(k_rope.shape) != (plan.total_kv, 64) or k_rope.stride(1) != 1:
         raise ValueError("k_rope must be a [T_kv, 64] view with unit column stride")
-    if k_rope.dtype != torch.bfloat16 or not k_rope.is_cuda:
-        raise TypeError("k_rope must be a bf16 CUDA tensor")
     if merge and (o is None or lse is None):
         raise ValueError("merge needs the partial state o and lse")
+    if k_rope.dtype != torch.bfloat16 or not k_rope.is_cuda:
+        raise TypeError("k_rope must be a bf16 CUDA tensor")
     if o is None:
         o = torch.empty((plan.total_q, H, 128), dtype=torch.bfloat16, device=q.device)
     if lse is None:

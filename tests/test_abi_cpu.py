@@ -182,3 +182,43 @@ def test_bindings_check_shapes_before_any_call():
         _binding.mla_merge_state(oa, la, torch.zeros(9, 2, 128, dtype=bf), la)
     with pytest.raises(ValueError):   # merge: lse_b of the wrong shape
         _binding.mla_merge_state(oa, la, oa, torch.zeros(10, 3))
+
+
+def test_new_entry_points_reject_bad_arguments_on_the_host():
+    """Argument checks of the paged, split, shared-rope and fp8 entry points: nothing is
+    launched (no GPU is needed to see the codes)."""
+    lib = mla.library()
+    # paged up-projection: only 576-wide entries; empty chunk is a no-op; null pointers rejected
+    assert lib.mla_up_proj_paged(None, 4, 64, 512, None, 1, None, None, 1, 8, None, 4, None, None, None, None) == -3
+    assert lib.mla_up_proj_paged(None, 4, 64, 576, None, 1, None, None, 1, 0, None, 4, None, None, None, None) == 0
+    assert lib.mla_up_proj_paged(None, 4, 64, 576, None, 1, None, None, 1, 8, None, 4, None, None, None, None) == -1
+    assert lib.mla_up_proj_paged(None, 4, 64, 576, None, 1, None, None, 0, 8, None, 4, None, None, None, None) == -2
+    # slots must fit a 32-bit TMA row coordinate
+    assert lib.mla_up_proj_paged(None, 1 << 26, 64, 576, None, 1, None, None, 1, 8, None, 4, None, None, None,
+                                 None) == -3
+    # split form: the rope output is required
+    assert lib.mla_up_proj_paged_split(None, 4, 64, 576, None, 1, None, None, 1, 8, None, 4, None, None, None, None,
+                                       None) == -1
+    # fp8 gather: only 648-byte entries; misaligned output rejected
+    assert lib.mla_gather_latent_fp8(None, 4, 64, 656, None, 1, None, None, 1, 8, None, None, None) == -3
+    assert lib.mla_gather_latent_fp8(None, 4, 64, 648, None, 1, None, None, 1, 0, None, None, None) == 0
+    assert lib.mla_gather_latent_fp8(8, 4, 64, 648, 16, 1, 16, 16, 1, 8, 24, None, None) == -1
+    # shared-rope run: a null plan is rejected
+    assert lib.mla_prefill_run_shared_rope(None, None, None, None, 64, None, None, None, 0, None) == -1
+
+
+def test_shared_rope_binding_checks_shapes():
+    import torch
+    from chunked_prefill_attention_ragged_gb300 import _binding
+
+    class FakePlan:   # only the fields the wrapper reads before any library call
+        num_heads, total_q, total_kv, handle = 2, 10, 20, None
+    bf = torch.bfloat16
+    q, kn, v = torch.zeros(10, 2, 192, dtype=bf), torch.zeros(20, 2, 128, dtype=bf), torch.zeros(20, 2, 128, dtype=bf)
+    with pytest.raises(ValueError):   # rope of the wrong width
+        _binding.mla_prefill_run_shared_rope(FakePlan(), q, kn, torch.zeros(20, 32, dtype=bf), v)
+    with pytest.raises(ValueError):   # K_nope with the rope still attached
+        _binding.mla_prefill_run_shared_rope(FakePlan(), q, torch.zeros(20, 2, 192, dtype=bf),
+                                             torch.zeros(20, 64, dtype=bf), v)
+    with pytest.raises(ValueError):   # merge without the partial state
+        _binding.mla_prefill_run_shared_rope(FakePlan(), q, kn, torch.zeros(20, 64, dtype=bf), v, merge=True)
