@@ -141,6 +141,7 @@ class PrefillPlan:
     num_ctas = property(lambda self: self.query(1))
     allowed_pairs = property(lambda self: self.query(4))
     kv_tiles = property(lambda self: self.query(5))
+    cta_pairs = property(lambda self: bool(self.query(6)))
 
     def run(self, q, k, v, o=None, lse=None, return_lse=True, stream=None):
         return mla_prefill_run(self, q, k, v, o, lse, return_lse, stream)

@@ -6,14 +6,20 @@
 // causal for new tokens / non-causal for prefix chunks, sm_scale, window_left,
 // logits_soft_cap; FlashInferPrefillImpl.run_prefill_*: O and LSE per (row, head)).
 //
-// Design (one persistent CTA per SM, one work unit = 128 query rows of one head; four
-// warpgroups, registers moved between them with setmaxnreg):
+// Design (persistent, one CTA per SM, four warpgroups, registers moved between them with
+// setmaxnreg).  A work unit is 128 query rows of one head (kPair = false), or 256 rows of
+// one head run by the two CTAs of a cluster (kPair): each CTA owns 128 of the rows, and
+// the pair's tensor-core products (tcgen05 cta_group::2, M = 256) read each K and V tile
+// half from either CTA, so every CTA loads half of the K/V bytes and its rings hold four
+// stages instead of two.
 //   warps 0, 2  TMA producers: warp 0 loads the Q tile once per unit and K tiles of 128
-//               keys, warp 2 V tiles, each through a two-stage ring.
-//   warps 1, 3  MMA issuers (one thread each): warp 1 issues S = Q K^T into one of three
-//               TMEM S buffers (tcgen05.mma, both operands from shared memory), so S
-//               runs up to two tiles ahead of the softmax; warp 3 issues O += P V with
-//               P read from TMEM (written there by the softmax warps over the S buffer).
+//               keys (a CTA of a pair: its 64 of them), warp 2 V tiles (a CTA of a pair:
+//               its 64 of the 128 value columns).
+//   warps 1, 3  MMA issuers (one thread each; in a pair only in the even CTA): warp 1
+//               issues S = Q K^T into one of three TMEM S buffers (both operands from
+//               shared memory), so S runs up to two tiles ahead of the softmax; warp 3
+//               issues O += P V with P read from TMEM.  In the odd CTA of a pair these
+//               warps forward its own Q/K and V arrivals to the even CTA's barriers.
 //   warps 4-11  softmax: two threads per query row (= one TMEM lane), each owning 64
 //               of the tile's 128 key columns and 64 of O's 128 columns.  Online
 //               softmax in base 2; O in TMEM is rescaled only when the running max
@@ -38,33 +44,46 @@
 namespace mla {
 namespace {
 
-constexpr int BM = kTileM;    // 128 query rows
-constexpr int BN = kTileN;    // 128 keys
+constexpr int BM = kTileM;    // 128 query rows per CTA
+constexpr int BN = kTileN;    // 128 keys per tile
 constexpr int PANEL = 128 * 64 * 2;   // one 128-row x 64-element bf16 panel, 128B swizzle
-constexpr int Q_PANELS = 3, K_PANELS = 3, V_PANELS = 2;
-constexpr int NSTAGE = 2;
-
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + Q_PANELS * PANEL;
-constexpr int OFF_V = OFF_K + NSTAGE * K_PANELS * PANEL;
-constexpr int OFF_BAR = OFF_V + NSTAGE * V_PANELS * PANEL;
+constexpr int Q_PANELS = 3, K_PANELS = 3;
 constexpr int NSB = 3;   // S buffers in TMEM
+
+// Shared-memory layout.  One CTA per unit: K and V tiles of 128 keys, two stages each.  A
+// CTA pair per unit: each CTA holds 64 keys of every K tile and 64 of the 128 value
+// columns of every V tile, four stages each.
+template <bool kPair>
+struct Lay {
+  static constexpr int KROWS = kPair ? 64 : 128;                 // keys of a K tile held here
+  static constexpr int KPANEL = KROWS * 64 * 2;                   // one 64-column K panel
+  static constexpr int V_PANELS = kPair ? 1 : 2;                  // 64-column V panels held here
+  static constexpr int NK = kPair ? 4 : 2, NV = kPair ? 4 : 2;   // stages
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + Q_PANELS * PANEL;
+  static constexpr int OFF_V = OFF_K + NK * K_PANELS * KPANEL;
+  static constexpr int OFF_BAR = OFF_V + NV * V_PANELS * PANEL;
+};
+constexpr int MAX_STAGES = 4;
 enum Bar {
-  QF = 0, QE = 1,       // Q landed / released
-  KF = 2, KE = 4,       // [stage] K tile landed / released
-  VF = 6,               // [stage] V tile landed
-  VE = 8,               // [stage] V tile released
-  SF = 10,              // [S buffer] S = Q K^T done
-  SE = 13,              // [S buffer] P V done reading P: S may be overwritten
-  OD = 16,              // [tile parity] O += P V done
-  FINQ = 18, FINP = 19, // all MMAs of each issuer drained before TMEM is released
-  XM = 20,              // [tile parity] softmax half-row max exchange
-  PR = 22,              // [S buffer] P written by all 8 softmax warps
-  LR = 25,              // [unit parity] row sums and max of a unit published
-  LFR = 27,             // [unit parity] the epilogue has read them
-  OFR = 29,             // the epilogue has read O: the next unit's first P V may overwrite it
-  NEVER = 30,           // nothing arrives here: the time-out test mode waits on it
-  NBAR = 31
+  QF = 0, QE = 1,       // Q landed (in a pair's even CTA: both CTAs' Q) / released
+  KF = 2,               // [stage] K tile landed (a pair's even CTA: both halves)
+  KE = KF + MAX_STAGES, // [stage] K tile released
+  VF = KE + MAX_STAGES, // [stage] V tile landed (a pair's even CTA: both halves)
+  VE = VF + MAX_STAGES, // [stage] V tile released
+  SF = VE + MAX_STAGES, // [S buffer] S = Q K^T done
+  SE = SF + NSB,        // [S buffer] P V done reading P: S may be overwritten
+  OD = SE + NSB,        // [tile parity] O += P V done
+  FINQ = OD + 2,        // all MMAs of the S issuer drained before TMEM is released
+  FINP,                 // the same for the P V issuer
+  XM,                   // [tile parity] softmax half-row max exchange (two barriers)
+  PR = XM + 2,          // [S buffer] P written by every softmax warp (of both CTAs of a pair)
+  LR = PR + NSB,        // [unit parity] row sums and max of a unit published
+  LFR = LR + 2,         // [unit parity] the epilogue has read them
+  OFR = LFR + 2,        // the epilogue (of both CTAs of a pair) has read O: the next
+                        // unit's first P V may overwrite it
+  NEVER,                // nothing arrives here: the time-out test mode waits on it
+  NBAR
 };
 // Parity waits: a wait for phase f of a barrier is exact only while phase f - 1 has
 // completed and phase f + 1 cannot have.  O-done is split by tile parity so that the
@@ -74,9 +93,13 @@ enum Bar {
 // epilogue's release of O) not yet given.
 // Exchange area: row max per (tile parity, half) and, per unit parity, both halves'
 // row sums and the row max, 10 x 128 floats.
-constexpr int OFF_XCHG = OFF_BAR + NBAR * 8;
-constexpr int OFF_MISC = OFF_XCHG + 10 * 128 * 4;
-constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + slack for 1024-byte alignment
+template <bool kPair>
+struct Off {
+  static constexpr int XCHG = Lay<kPair>::OFF_BAR + NBAR * 8;
+  static constexpr int MISC = XCHG + 10 * 128 * 4;
+  static constexpr int SMEM = MISC + 16 + 1024;   // + slack for 1024-byte alignment
+};
+static_assert(Off<false>::SMEM <= 227 * 1024 && Off<true>::SMEM <= 227 * 1024, "shared memory budget");
 
 constexpr int NTHREADS = 512;   // 4 warpgroups: control, softmax x 2, epilogue
 // Registers per thread: launched at 65536 / 512 = 128; the control and epilogue
@@ -93,24 +116,54 @@ constexpr uint32_t TMEM_COLS = 512;
 __device__ __forceinline__ constexpr uint32_t TM_S(int b) { return (uint32_t)b * 128u; }
 constexpr uint32_t TM_O = 384;
 
-constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false, false);
-constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, 128, false, true);
+// M = 128 rows per CTA, or 256 over a pair; N = 128 keys (S) or 128 value columns (P V).
+template <bool kPair>
+struct Idesc {
+  static constexpr uint32_t QK = idesc_bf16_f32(kPair ? 256 : BM, BN, false, false);
+  static constexpr uint32_t PV = idesc_bf16_f32(kPair ? 256 : BM, 128, false, true);
+};
 
 constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;    // 0.2 s: own copies and MMAs after an abort
 constexpr float RESCALE_THRESHOLD = 8.0f;             // log2 units
 
+template <bool kPair>
 struct Ctx {
   uint32_t sbase;
   volatile int* abort_flag;
   int* status;
   uint64_t wait_limit_ns;
-  __device__ uint32_t bar(int i) const { return sbase + OFF_BAR + 8 * i; }
+  uint32_t rank;   // the CTA's rank in its pair (0 without pairs)
+  __device__ uint32_t bar(int i) const { return sbase + Lay<kPair>::OFF_BAR + 8 * i; }
   __device__ bool wait(int b, uint32_t parity) const {
     return mbar_wait_bounded(bar(b), parity, abort_flag, status, MLA_DEVSTAT_TIMEOUT, wait_limit_ns);
   }
+  // For barriers that threads of the other CTA of a pair arrive on (the even CTA's Q/K/V
+  // landed, P written and O read barriers): acquire at cluster scope.
+  __device__ bool wait_pair(int b, uint32_t parity) const {
+    return mbar_wait_bounded(bar(b), parity, abort_flag, status, MLA_DEVSTAT_TIMEOUT, wait_limit_ns, kPair);
+  }
   __device__ void drain(int b, uint32_t parity) const {
     int dummy = 0;
-    mbar_wait_bounded(bar(b), parity, &dummy, status, MLA_DEVSTAT_TIMEOUT, DRAIN_LIMIT_NS);
+    mbar_wait_bounded(bar(b), parity, &dummy, status, MLA_DEVSTAT_TIMEOUT, DRAIN_LIMIT_NS, kPair);
+  }
+  // Arrive on barrier b of the even CTA of the pair (this CTA's own without pairs).
+  __device__ void arrive_leader(int b) const {
+    if (kPair && rank != 0)
+      mbar_arrive_remote(mapa_shared(bar(b), 0));
+    else
+      mbar_arrive(bar(b));
+  }
+  // Commit this thread's tensor-core work to barrier b of this CTA, or of both CTAs of a pair.
+  __device__ void commit(int b) const {
+    if constexpr (kPair) tc_commit_pair(bar(b)); else tc_commit(bar(b));
+  }
+  __device__ void commit_both(int b) const {
+    if constexpr (kPair) {
+      tc_commit_pair(bar(b));
+      tc_commit_pair(mapa_shared(bar(b), 1));
+    } else {
+      tc_commit(bar(b));
+    }
   }
 };
 
@@ -123,12 +176,31 @@ __device__ __forceinline__ Unit load_unit(const Unit* units, int i) {
   return u;
 }
 
+// The unit's query rows that this CTA owns: all of them without pairs (at most 128); in a
+// pair the first 128 for the even CTA and the rest (possibly none) for the odd one.
+template <bool kPair>
+__device__ __forceinline__ Unit own_rows(Unit u, uint32_t rank) {
+  if constexpr (kPair) {
+    if (rank != 0) {
+      u.q_row0 += BM;
+      u.q_pos0 += BM;
+      u.q_rows = u.q_rows > BM ? u.q_rows - BM : 0;
+    } else if (u.q_rows > BM) {
+      u.q_rows = BM;
+    }
+  }
+  return u;
+}
+
 // ------------------------------------------------------------------ producers
 // Two producer threads, so that a K load never queues behind a V load waiting for its
 // stage: warp 0 loads Q (once per unit) and K tiles, warp 2 loads V tiles.  A K stage
-// frees when its S = Q K^T is done, a V stage when its P V is done.
-__device__ void run_producer_qk(const Ctx& c, const PrefillParams& p, const CUtensorMap* tq,
+// frees when its S = Q K^T is done, a V stage when its P V is done.  In a pair each CTA
+// loads its own Q rows, its half of the K tile's keys and its half of V's columns.
+template <bool kPair>
+__device__ void run_producer_qk(const Ctx<kPair>& c, const PrefillParams& p, const CUtensorMap* tq,
                                 const CUtensorMap* tk, const CUtensorMap* tr, int ubeg, int uend) {
+  using L = Lay<kPair>;
   int q_g = 0, k_g = 0;   // loads issued so far (Q tiles, K tiles)
   bool ok = true;
   for (int ui = ubeg; ui < uend && ok; ++ui) {
@@ -137,19 +209,20 @@ __device__ void run_producer_qk(const Ctx& c, const PrefillParams& p, const CUte
     if (hi <= lo) continue;
     if (q_g > 0 && !c.wait(QE, (q_g - 1) & 1)) { ok = false; break; }
     mbar_arrive_expect_tx(c.bar(QF), Q_PANELS * PANEL);
+    const int q_row = u.q_row0 + (kPair ? BM * (int)c.rank : 0);
     for (int i = 0; i < Q_PANELS; ++i)
-      tma_load_3d(c.sbase + OFF_Q + i * PANEL, tq, c.bar(QF), i * 64, u.head, u.q_row0);
+      tma_load_3d(c.sbase + L::OFF_Q + i * PANEL, tq, c.bar(QF), i * 64, u.head, q_row);
     ++q_g;
     for (int t = lo; t < hi; ++t) {
-      const int row = u.kv_row0 + t * BN;
-      const int s = k_g % NSTAGE;
-      const uint32_t use = k_g / NSTAGE;
+      const int row = u.kv_row0 + t * BN + (kPair ? L::KROWS * (int)c.rank : 0);
+      const int s = k_g % L::NK;
+      const uint32_t use = k_g / L::NK;
       if (use > 0 && !c.wait(KE + s, (use - 1) & 1)) { ok = false; break; }
-      mbar_arrive_expect_tx(c.bar(KF + s), K_PANELS * PANEL);
+      mbar_arrive_expect_tx(c.bar(KF + s), K_PANELS * L::KPANEL);
       // Panels 0-1 are K's NoPE columns; panel 2 its RoPE columns, which with a shared
       // rope come from the one [tokens, 64] rope tensor that every head uses.
       for (int i = 0; i < K_PANELS; ++i) {
-        const uint32_t dst = c.sbase + OFF_K + (s * K_PANELS + i) * PANEL;
+        const uint32_t dst = c.sbase + L::OFF_K + (s * K_PANELS + i) * L::KPANEL;
         if (p.shared_rope && i == K_PANELS - 1)
           tma_load_2d(dst, tr, c.bar(KF + s), 0, row);
         else
@@ -161,12 +234,14 @@ __device__ void run_producer_qk(const Ctx& c, const PrefillParams& p, const CUte
   // Let every copy this thread started land before the CTA can exit: wait for the
   // last phase issued on each barrier (already complete on the normal path).
   if (q_g > 0) c.drain(QF, (q_g - 1) & 1);
-  for (int s = 0; s < NSTAGE; ++s)
-    if (k_g > s) c.drain(KF + s, (((k_g - 1 - s) / NSTAGE)) & 1);
+  for (int s = 0; s < L::NK; ++s)
+    if (k_g > s) c.drain(KF + s, (((k_g - 1 - s) / L::NK)) & 1);
 }
 
-__device__ void run_producer_v(const Ctx& c, const PrefillParams& p, const CUtensorMap* tv, int ubeg,
+template <bool kPair>
+__device__ void run_producer_v(const Ctx<kPair>& c, const PrefillParams& p, const CUtensorMap* tv, int ubeg,
                                int uend) {
+  using L = Lay<kPair>;
   int v_g = 0;
   bool ok = true;
   for (int ui = ubeg; ui < uend && ok; ++ui) {
@@ -174,17 +249,52 @@ __device__ void run_producer_v(const Ctx& c, const PrefillParams& p, const CUten
     const int lo = u.kv_tiles & 0xFFFF, hi = (u.kv_tiles >> 16) & 0xFFFF;
     for (int t = lo; t < hi; ++t) {
       const int row = u.kv_row0 + t * BN;
-      const int s = v_g % NSTAGE;
-      const uint32_t use = v_g / NSTAGE;
+      const int s = v_g % L::NV;
+      const uint32_t use = v_g / L::NV;
       if (use > 0 && !c.wait(VE + s, (use - 1) & 1)) { ok = false; break; }
-      mbar_arrive_expect_tx(c.bar(VF + s), V_PANELS * PANEL);
-      for (int i = 0; i < V_PANELS; ++i)
-        tma_load_3d(c.sbase + OFF_V + (s * V_PANELS + i) * PANEL, tv, c.bar(VF + s), i * 64, u.head, row);
+      mbar_arrive_expect_tx(c.bar(VF + s), L::V_PANELS * PANEL);
+      for (int i = 0; i < L::V_PANELS; ++i)
+        tma_load_3d(c.sbase + L::OFF_V + (s * L::V_PANELS + i) * PANEL, tv, c.bar(VF + s),
+                    kPair ? 64 * (int)c.rank : i * 64, u.head, row);
       ++v_g;
     }
   }
-  for (int s = 0; s < NSTAGE; ++s)
-    if (v_g > s) c.drain(VF + s, (((v_g - 1 - s) / NSTAGE)) & 1);
+  for (int s = 0; s < L::NV; ++s)
+    if (v_g > s) c.drain(VF + s, (((v_g - 1 - s) / L::NV)) & 1);
+}
+
+// The odd CTA of a pair: once its own Q / K half / V half of a tile has landed, tell the
+// even CTA, whose MMA issuers wait for both CTAs' halves on their own barriers.
+__device__ void run_forward_qk(const Ctx<true>& c, const PrefillParams& p, int ubeg, int uend) {
+  using L = Lay<true>;
+  int q_g = 0, k_g = 0;
+  for (int ui = ubeg; ui < uend; ++ui) {
+    const Unit u = load_unit(p.units, ui);
+    const int lo = u.kv_tiles & 0xFFFF, hi = (u.kv_tiles >> 16) & 0xFFFF;
+    if (hi <= lo) continue;
+    if (!c.wait(QF, q_g & 1)) return;
+    mbar_arrive_remote(mapa_shared(c.bar(QF), 0));
+    ++q_g;
+    for (int t = lo; t < hi; ++t, ++k_g) {
+      const int s = k_g % L::NK;
+      if (!c.wait(KF + s, (k_g / L::NK) & 1)) return;
+      mbar_arrive_remote(mapa_shared(c.bar(KF + s), 0));
+    }
+  }
+}
+
+__device__ void run_forward_v(const Ctx<true>& c, const PrefillParams& p, int ubeg, int uend) {
+  using L = Lay<true>;
+  int v_g = 0;
+  for (int ui = ubeg; ui < uend; ++ui) {
+    const Unit u = load_unit(p.units, ui);
+    const int lo = u.kv_tiles & 0xFFFF, hi = (u.kv_tiles >> 16) & 0xFFFF;
+    for (int t = lo; t < hi; ++t, ++v_g) {
+      const int s = v_g % L::NV;
+      if (!c.wait(VF + s, (v_g / L::NV) & 1)) return;
+      mbar_arrive_remote(mapa_shared(c.bar(VF + s), 0));
+    }
+  }
 }
 
 // ------------------------------------------------------------------ MMA issuer
@@ -192,12 +302,15 @@ __device__ void run_producer_v(const Ctx& c, const PrefillParams& p, const CUten
 // instruction, so every wait of an issuing thread leaves the pipe idle unless another
 // thread has products queued: warp 1 issues S = Q K^T, warp 3 issues O += P V, and
 // each one's waits hide behind the other's products.  S of tile g + 3 reuses the S
-// buffer whose P the product of tile g reads, which the SE barrier orders.
-__device__ void run_mma_qk(const Ctx& c, const PrefillParams& p, uint32_t tmem, int ubeg, int uend) {
+// buffer whose P the product of tile g reads, which the SE barrier orders.  In a pair
+// the even CTA issues for both, and commits the barriers of both CTAs.
+template <bool kPair>
+__device__ void run_mma_qk(const Ctx<kPair>& c, const PrefillParams& p, uint32_t tmem, int ubeg, int uend) {
+  using L = Lay<kPair>;
   int q_g = 0, kv_g = 0;
   bool ok = true;
-  const uint64_t q_desc = sdesc_sw128(c.sbase + OFF_Q, 16, 1024);
-  const uint64_t k_desc0 = sdesc_sw128(c.sbase + OFF_K, 16, 1024);
+  const uint64_t q_desc = sdesc_sw128(c.sbase + L::OFF_Q, 16, 1024);
+  const uint64_t k_desc0 = sdesc_sw128(c.sbase + L::OFF_K, 16, 1024);
   // Time-out test mode: phase 0 of NEVER never completes, so this wait gives up after
   // the plan's limit and the whole CTA takes its abort path.
   if (p.force_timeout) ok = c.wait(NEVER, 0);
@@ -206,34 +319,40 @@ __device__ void run_mma_qk(const Ctx& c, const PrefillParams& p, uint32_t tmem, 
     const int lo = u.kv_tiles & 0xFFFF, hi = (u.kv_tiles >> 16) & 0xFFFF;
     const int n = hi - lo;
     if (n <= 0) continue;
-    if (!c.wait(QF, q_g & 1)) { ok = false; break; }
+    if (!c.wait_pair(QF, q_g & 1)) { ok = false; break; }
     ++q_g;
     for (int j = 0; j < n && ok; ++j) {
-      const int g = kv_g + j, s = g % NSTAGE, b = g % NSB;
-      if (!c.wait(KF + s, (g / NSTAGE) & 1)) { ok = false; break; }
+      const int g = kv_g + j, s = g % L::NK, b = g % NSB;
+      if (!c.wait_pair(KF + s, (g / L::NK) & 1)) { ok = false; break; }
       if (g >= NSB && !c.wait(SE + b, ((g - NSB) / NSB) & 1)) { ok = false; break; }
       tc_fence_after();
-      const uint64_t kd = k_desc0 + (uint64_t)(s * K_PANELS * PANEL >> 4);
+      const uint64_t kd = k_desc0 + (uint64_t)(s * K_PANELS * L::KPANEL >> 4);
 #pragma unroll
       for (int kk = 0; kk < 192 / 16; ++kk) {
-        const uint64_t off = (uint64_t)(((kk >> 2) * PANEL + (kk & 3) * 32) >> 4);
-        mma_ss(tmem + TM_S(b), q_desc + off, kd + off, IDESC_QK, kk > 0 ? 1u : 0u);
+        const uint64_t q_off = (uint64_t)(((kk >> 2) * PANEL + (kk & 3) * 32) >> 4);
+        const uint64_t k_off = (uint64_t)(((kk >> 2) * L::KPANEL + (kk & 3) * 32) >> 4);
+        if constexpr (kPair)
+          mma_ss_pair(tmem + TM_S(b), q_desc + q_off, kd + k_off, Idesc<kPair>::QK, kk > 0 ? 1u : 0u);
+        else
+          mma_ss(tmem + TM_S(b), q_desc + q_off, kd + k_off, Idesc<kPair>::QK, kk > 0 ? 1u : 0u);
       }
-      tc_commit(c.bar(SF + b));
-      tc_commit(c.bar(KE + s));
-      if (j == n - 1) tc_commit(c.bar(QE));
+      c.commit_both(SF + b);
+      c.commit_both(KE + s);
+      if (j == n - 1) c.commit_both(QE);
     }
     kv_g += n;
   }
   // Every MMA issued by this thread must finish before TMEM is released.
-  tc_commit(c.bar(FINQ));
+  c.commit(FINQ);
   c.drain(FINQ, 0);
 }
 
-__device__ void run_mma_pv(const Ctx& c, const PrefillParams& p, uint32_t tmem, int ubeg, int uend) {
+template <bool kPair>
+__device__ void run_mma_pv(const Ctx<kPair>& c, const PrefillParams& p, uint32_t tmem, int ubeg, int uend) {
+  using L = Lay<kPair>;
   int g = 0, k = 0;   // tiles and non-empty units so far
   bool ok = true;
-  const uint64_t v_desc0 = sdesc_sw128(c.sbase + OFF_V, PANEL, 1024);
+  const uint64_t v_desc0 = sdesc_sw128(c.sbase + L::OFF_V, PANEL, 1024);
   for (int ui = ubeg; ui < uend && ok; ++ui) {
     const Unit u = load_unit(p.units, ui);
     const int lo = u.kv_tiles & 0xFFFF, hi = (u.kv_tiles >> 16) & 0xFFFF;
@@ -241,24 +360,29 @@ __device__ void run_mma_pv(const Ctx& c, const PrefillParams& p, uint32_t tmem, 
     if (n <= 0) continue;
     // The first product of a unit overwrites O: the epilogue must have read the
     // previous unit's O out of TMEM.
-    if (k > 0 && !c.wait(OFR, (k - 1) & 1)) { ok = false; break; }
+    if (k > 0 && !c.wait_pair(OFR, (k - 1) & 1)) { ok = false; break; }
     ++k;
     for (int j = 0; j < n; ++j, ++g) {
       // Tiles are counted alike for S buffers and V stages (both advance once per tile).
-      const int b = g % NSB, s = g % NSTAGE;
-      if (!c.wait(PR + b, (g / NSB) & 1) || !c.wait(VF + s, (g / NSTAGE) & 1)) { ok = false; break; }
+      const int b = g % NSB, s = g % L::NV;
+      if (!c.wait_pair(PR + b, (g / NSB) & 1) || !c.wait_pair(VF + s, (g / L::NV) & 1)) { ok = false; break; }
       tc_fence_after();
-      const uint64_t vd = v_desc0 + (uint64_t)(s * V_PANELS * PANEL >> 4);
+      const uint64_t vd = v_desc0 + (uint64_t)(s * L::V_PANELS * PANEL >> 4);
 #pragma unroll
-      for (int kk = 0; kk < BN / 16; ++kk)
-        mma_ts(tmem + TM_O, tmem + TM_S(b) + kk * 8, vd + (uint64_t)(kk * 16 * 128 >> 4), IDESC_PV,
-               (j > 0 || kk > 0) ? 1u : 0u);
-      tc_commit(c.bar(VE + s));
-      tc_commit(c.bar(SE + b));
-      tc_commit(c.bar(OD + (g & 1)));
+      for (int kk = 0; kk < BN / 16; ++kk) {
+        if constexpr (kPair)
+          mma_ts_pair(tmem + TM_O, tmem + TM_S(b) + kk * 8, vd + (uint64_t)(kk * 16 * 128 >> 4), Idesc<kPair>::PV,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        else
+          mma_ts(tmem + TM_O, tmem + TM_S(b) + kk * 8, vd + (uint64_t)(kk * 16 * 128 >> 4), Idesc<kPair>::PV,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+      }
+      c.commit_both(VE + s);
+      c.commit(SE + b);
+      c.commit_both(OD + (g & 1));
     }
   }
-  tc_commit(c.bar(FINP));
+  c.commit(FINP);
   c.drain(FINP, 0);
 }
 
@@ -268,8 +392,8 @@ __device__ void run_mma_pv(const Ctx& c, const PrefillParams& p, uint32_t tmem, 
 // all 128 rows).  The halves agree on the row max through shared memory once per tile;
 // at the end of a unit each publishes its row sum (and half 0 the row max) for the
 // epilogue warps.  Every exchange sits behind an mbarrier so every wait stays bounded.
-template <bool kMerge>
-__device__ void run_softmax(const Ctx& c, const PrefillParams& p, uint32_t tmem, float* xchg,
+template <bool kMerge, bool kPair>
+__device__ void run_softmax(const Ctx<kPair>& c, const PrefillParams& p, uint32_t tmem, float* xchg,
                             int ubeg, int uend) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;                 // TMEM lanes this warp may touch
@@ -283,7 +407,7 @@ __device__ void run_softmax(const Ctx& c, const PrefillParams& p, uint32_t tmem,
   const float NEG_INF = -__int_as_float(0x7f800000);
   const float2 sc2 = make_float2(p.has_cap ? 1.f : p.scale_log2, p.has_cap ? 1.f : p.scale_log2);
   for (int ui = ubeg; ui < uend && ok; ++ui) {
-    const Unit u = load_unit(p.units, ui);
+    const Unit u = own_rows<kPair>(load_unit(p.units, ui), c.rank);
     const int lo = u.kv_tiles & 0xFFFF, hi = (u.kv_tiles >> 16) & 0xFFFF;
     const int n = hi - lo;
     const int qpos = u.q_pos0 + row;
@@ -397,7 +521,7 @@ __device__ void run_softmax(const Ctx& c, const PrefillParams& p, uint32_t tmem,
       m_used = m_new;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(PR + b));
+      if (lane == 0) c.arrive_leader(PR + b);
     }
     if (!ok) break;
     // Hand the unit to the epilogue warps: this half's row sum and the row max.  The
@@ -500,8 +624,8 @@ __device__ __forceinline__ void store_row(char* dst, int align32, const uint32_t
 // P V; read O, release it to the P V issuer, and store.  The stores are row per thread
 // (eight 32-byte stores of 256 contiguous bytes): off the softmax's critical path, a
 // shuffle exchange that would coalesce them costs more issue slots than it saves.
-template <bool kMerge>
-__device__ void run_epilogue(const Ctx& c, const PrefillParams& p, uint32_t tmem, const float* xchg,
+template <bool kMerge, bool kPair>
+__device__ void run_epilogue(const Ctx<kPair>& c, const PrefillParams& p, uint32_t tmem, const float* xchg,
                              int ubeg, int uend) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quad = warp & 3;
@@ -511,7 +635,7 @@ __device__ void run_epilogue(const Ctx& c, const PrefillParams& p, uint32_t tmem
   const float NEG_INF = -__int_as_float(0x7f800000);
   int g = 0, k = 0;   // tiles and non-empty units so far
   for (int ui = ubeg; ui < uend; ++ui) {
-    const Unit u = load_unit(p.units, ui);
+    const Unit u = own_rows<kPair>(load_unit(p.units, ui), c.rank);
     const int lo = u.kv_tiles & 0xFFFF, hi = (u.kv_tiles >> 16) & 0xFFFF;
     const int n = hi - lo;
     if (n <= 0) continue;
@@ -538,7 +662,7 @@ __device__ void run_epilogue(const Ctx& c, const PrefillParams& p, uint32_t tmem
       load_scaled_half(lane_addr + TM_O + 64, inv, w1);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(OFR));
+      if (lane == 0) c.arrive_leader(OFR);
       // (The row address is formed twice on purpose: holding it across the stores
       // costs registers this warpgroup does not have.)
       if (live)
@@ -574,7 +698,7 @@ __device__ void run_epilogue(const Ctx& c, const PrefillParams& p, uint32_t tmem
       load_scaled_half(lane_addr + TM_O + 64, b, w1);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(OFR));
+      if (lane == 0) c.arrive_leader(OFR);
       if (live) {
         // A side with LSE = -inf gets weight 0 and its O is never read.  One half at a
         // time, merged then stored (the barrier keeps the second half's loads below the
@@ -596,7 +720,8 @@ __device__ void run_epilogue(const Ctx& c, const PrefillParams& p, uint32_t tmem
 }
 
 // kMerge: o/lse hold a partial state that the epilogue merges this attention into.
-template <bool kMerge>
+// kPair: launched as clusters of two CTAs, unit lists indexed by cluster.
+template <bool kMerge, bool kPair>
 __global__ void __launch_bounds__(NTHREADS, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
@@ -604,9 +729,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
-  int* abort_flag = reinterpret_cast<int*>(smem + OFF_MISC + 4);
-  Ctx c{smem_addr(smem), abort_flag, p.status, p.wait_limit_ns};
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Off<kPair>::MISC);
+  int* abort_flag = reinterpret_cast<int*>(smem + Off<kPair>::MISC + 4);
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  Ctx<kPair> c{smem_addr(smem), abort_flag, p.status, p.wait_limit_ns, rank};
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBAR; ++i) mbar_init(c.bar(i), 1);
@@ -615,8 +741,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       mbar_init(c.bar(LR + i), 256);
       mbar_init(c.bar(LFR + i), 128);  // every epilogue thread
     }
-    for (int i = 0; i < NSB; ++i) mbar_init(c.bar(PR + i), 8);   // one arrival per softmax warp
-    mbar_init(c.bar(OFR), 4);                                      // one arrival per epilogue warp
+    // One arrival per softmax warp / epilogue warp, of both CTAs in a pair's even CTA.
+    const int both = kPair && rank == 0 ? 2 : 1;
+    for (int i = 0; i < NSB; ++i) mbar_init(c.bar(PR + i), 8 * both);
+    mbar_init(c.bar(OFR), 4 * both);
+    if (kPair && rank == 0) {   // own load (with its bytes) + the odd CTA's forwarded arrival
+      mbar_init(c.bar(QF), 2);
+      for (int s = 0; s < Lay<kPair>::NK; ++s) mbar_init(c.bar(KF + s), 2);
+      for (int s = 0; s < Lay<kPair>::NV; ++s) mbar_init(c.bar(VF + s), 2);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -627,69 +760,124 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (p.shared_rope) tma_prefetch_desc(&tm_r);
   }
   if (warp == 1) {
-    tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (kPair) {   // one warp of each CTA of the pair, together
+      tmem_alloc_pair(smem_addr(tmem_slot), TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) cluster_sync();   // both CTAs' barriers exist before any remote arrival
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int ubeg = p.cta_offsets[blockIdx.x], uend = p.cta_offsets[blockIdx.x + 1];
+  const int slot_idx = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int ubeg = p.cta_offsets[slot_idx], uend = p.cta_offsets[slot_idx + 1];
 
-  float* xchg = reinterpret_cast<float*>(smem + OFF_XCHG);
+  float* xchg = reinterpret_cast<float*>(smem + Off<kPair>::XCHG);
   if (warp < 4) {
     setmaxnreg_dec<RegSplit<kMerge>::ctrl>();
     if (lane == 0) {
-      if (warp == 0) run_producer_qk(c, p, &tm_q, &tm_k, &tm_r, ubeg, uend);
-      else if (warp == 1) run_mma_qk(c, p, tmem, ubeg, uend);
-      else if (warp == 2) run_producer_v(c, p, &tm_v, ubeg, uend);
-      else run_mma_pv(c, p, tmem, ubeg, uend);
+      const bool issuer = !kPair || rank == 0;
+      if (warp == 0) {
+        run_producer_qk<kPair>(c, p, &tm_q, &tm_k, &tm_r, ubeg, uend);
+      } else if (warp == 2) {
+        run_producer_v<kPair>(c, p, &tm_v, ubeg, uend);
+      } else if (issuer) {
+        if (warp == 1) run_mma_qk<kPair>(c, p, tmem, ubeg, uend);
+        else run_mma_pv<kPair>(c, p, tmem, ubeg, uend);
+      } else if constexpr (kPair) {
+        if (warp == 1) run_forward_qk(c, p, ubeg, uend);
+        else run_forward_v(c, p, ubeg, uend);
+      }
     }
   } else if (warp < 12) {
     setmaxnreg_inc<RegSplit<kMerge>::softmax>();
-    run_softmax<kMerge>(c, p, tmem, xchg, ubeg, uend);
+    run_softmax<kMerge, kPair>(c, p, tmem, xchg, ubeg, uend);
   } else {
     setmaxnreg_dec<RegSplit<kMerge>::epi>();
-    run_epilogue<kMerge>(c, p, tmem, xchg, ubeg, uend);
+    run_epilogue<kMerge, kPair>(c, p, tmem, xchg, ubeg, uend);
   }
   tc_fence_before();
   __syncthreads();
+  // In a pair, neither CTA leaves (freeing its shared memory and TMEM) while the even
+  // CTA's products may still read or write the other's.
+  if constexpr (kPair) cluster_sync();
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem, TMEM_COLS);
+    if constexpr (kPair) tmem_dealloc_pair(tmem, TMEM_COLS); else tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
 }  // namespace
 
-int prefill_smem_bytes() { return SMEM_BYTES; }
+int prefill_smem_bytes() { return Off<false>::SMEM; }
 
-template <bool kMerge>
+template <bool kMerge, bool kPair>
+static cudaError_t configure_prefill() {
+  cudaError_t r = cudaFuncSetAttribute(prefill_kernel<kMerge, kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Off<kPair>::SMEM);
+  if (r != cudaSuccess) return r;
+  // The warpgroups' setmaxnreg split assumes every thread starts with LAUNCH_REGS
+  // registers; with fewer, the softmax warpgroups' increase could never be granted.
+  cudaFuncAttributes attr;
+  r = cudaFuncGetAttributes(&attr, prefill_kernel<kMerge, kPair>);
+  if (r != cudaSuccess) return r;
+  return attr.numRegs == LAUNCH_REGS ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
+static cudaLaunchConfig_t pair_config(cudaLaunchAttribute* attr, int num_pairs, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * num_pairs, 1, 1);
+  cfg.blockDim = dim3(NTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = Off<true>::SMEM;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+int prefill_max_pairs() {
+  static PerDeviceOnce configured;
+  if (configured.run([] { return configure_prefill<false, true>(); }) != cudaSuccess) return 0;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pair_config(attr, 1, nullptr);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, prefill_kernel<false, true>, &cfg) != cudaSuccess) return 0;
+  return n;
+}
+
+template <bool kMerge, bool kPair>
 static cudaError_t launch_prefill_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                    const CUtensorMap& tr, const PrefillParams& p, int num_ctas,
+                                    const CUtensorMap& tr, const PrefillParams& p, int num_slots,
                                     cudaStream_t stream) {
   static PerDeviceOnce configured;
-  cudaError_t e = configured.run([] {
-    cudaError_t r = cudaFuncSetAttribute(prefill_kernel<kMerge>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SMEM_BYTES);
-    if (r != cudaSuccess) return r;
-    // The warpgroups' setmaxnreg split assumes every thread starts with LAUNCH_REGS
-    // registers; with fewer, the softmax warpgroups' increase could never be granted.
-    cudaFuncAttributes attr;
-    r = cudaFuncGetAttributes(&attr, prefill_kernel<kMerge>);
-    if (r != cudaSuccess) return r;
-    return attr.numRegs == LAUNCH_REGS ? cudaSuccess : cudaErrorInvalidConfiguration;
-  });
+  cudaError_t e = configured.run([] { return configure_prefill<kMerge, kPair>(); });
   if (e != cudaSuccess) return e;
-  prefill_kernel<kMerge><<<num_ctas, NTHREADS, SMEM_BYTES, stream>>>(tq, tk, tv, tr, p);
-  return cudaGetLastError();
+  if constexpr (kPair) {
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = pair_config(attr, num_slots, stream);
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<kMerge, true>, tq, tk, tv, tr, p);
+  } else {
+    prefill_kernel<kMerge, false><<<num_slots, NTHREADS, Off<false>::SMEM, stream>>>(tq, tk, tv, tr, p);
+    return cudaGetLastError();
+  }
 }
 
 cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const CUtensorMap& tr, const PrefillParams& p, int num_ctas, cudaStream_t stream) {
-  return p.merge ? launch_prefill_t<true>(tq, tk, tv, tr, p, num_ctas, stream)
-                 : launch_prefill_t<false>(tq, tk, tv, tr, p, num_ctas, stream);
+                           const CUtensorMap& tr, const PrefillParams& p, int num_slots, cudaStream_t stream) {
+  if (p.pair)
+    return p.merge ? launch_prefill_t<true, true>(tq, tk, tv, tr, p, num_slots, stream)
+                   : launch_prefill_t<false, true>(tq, tk, tv, tr, p, num_slots, stream);
+  return p.merge ? launch_prefill_t<true, false>(tq, tk, tv, tr, p, num_slots, stream)
+                 : launch_prefill_t<false, false>(tq, tk, tv, tr, p, num_slots, stream);
 }
 
 }  // namespace mla

@@ -32,6 +32,8 @@ struct PrefillParams {
   uint64_t wait_limit_ns;     // a pipeline wait gives up after this long (default 2 s)
   int force_timeout;          // test mode: one wait that nothing satisfies (see below)
   int shared_rope;            // K's RoPE columns come from one [kv rows, 64] tensor (map tm_r)
+  int pair;                   // units of 256 rows run by CTA pairs (clusters of two); the K
+                              // and rope maps then have 64-row boxes
 };
 
 // Time-out test mode.  When the environment variable MLA_TEST_FORCE_TIMEOUT_NS holds a
@@ -45,8 +47,10 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;   // the normal limit of a pipe
 
 int prefill_smem_bytes();
 // tr: the shared RoPE tensor's map when p.shared_rope is set (any valid map otherwise).
+// num_slots: CTAs, or CTA pairs when p.pair is set (the plan's cta_offsets has num_slots + 1
+// entries).
 cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const CUtensorMap& tr, const PrefillParams& p, int num_ctas, cudaStream_t stream);
+                           const CUtensorMap& tr, const PrefillParams& p, int num_slots, cudaStream_t stream);
 
 // ---- tensor maps (tma.cpp) ---------------------------------------------------
 // bf16 tensor of rank 2 or 3 (dims innermost first, strides in bytes for dims 1..),
@@ -84,6 +88,12 @@ cudaError_t launch_merge(const void* o_a, const float* lse_a, const void* o_b, c
                          cudaStream_t stream);
 
 int device_sm_count();
+
+// MLA_PLAN_CTA_PAIRS: 1 when "1" (plan prefills on CTA pairs), 0 when "0", -1 otherwise.
+int cta_pair_mode();
+
+// How many clusters of two prefill CTAs the current device runs at once (0 on error).
+int prefill_max_pairs();
 
 // Runs a set-up step (kernel attributes, symbol lookups) once per device, from any
 // number of host threads: the first caller on a device runs it under a lock, later

@@ -1,5 +1,6 @@
 // C ABI of the library (declared in include/mla_prefill.h): argument checks, the
 // plan object and its device workspace, tensor maps, kernel launches.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <new>
@@ -16,7 +17,8 @@ struct mla_plan {
   uint64_t forced_timeout_ns = 0;   // test mode (see forced_timeout_ns())
   int64_t total_q = 0, total_kv = 0;
   PlanResult plan;
-  int num_ctas = 0;
+  int num_ctas = 0;              // CTAs, or CTA pairs when pair is set
+  int pair = 0;                  // units of 256 rows, each run by a cluster of two CTAs
   void* workspace = nullptr;     // units | cta offsets | status word (stream-ordered allocation)
   cudaEvent_t last_use = nullptr;  // recorded after the upload and after every uncaptured run
   Unit* d_units = nullptr;
@@ -81,7 +83,8 @@ int mla_plan_units_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int 
                         int32_t* cta_offsets, int64_t* num_units) {
   if (!num_units || !cta_offsets || (capacity > 0 && !units) || num_ctas < 1) return MLA_ERR_INVALID_ARG;
   PlanResult pr;
-  const int rc = build_plan(qo_indptr, kv_indptr, batch, num_heads, causal != 0, window_left, num_ctas, &pr);
+  const int rows = cta_pair_mode() == 1 ? 2 * kTileM : kTileM;
+  const int rc = build_plan(qo_indptr, kv_indptr, batch, num_heads, causal != 0, window_left, num_ctas, &pr, rows);
   if (rc != MLA_OK) return rc;
   *num_units = (int64_t)pr.units.size();
   if ((int64_t)pr.units.size() > capacity) return MLA_ERR_SHAPE;
@@ -114,6 +117,17 @@ int mla_prefill_plan(mla_plan_t* out, const int32_t* qo_indptr, const int32_t* k
   if (!p) return MLA_ERR_CUDA;
   int rc = build_plan(qo_indptr, kv_indptr, batch, num_heads, causal != 0, window_left, sms, &p->plan);
   if (rc != MLA_OK) { delete p; return rc; }
+  // CTA pairs only on request: on every batch shape measured they ran 3-10% slower than
+  // single CTAs (the pair relieves shared-memory bandwidth, but its tiles wait on the same
+  // softmax-to-MMA chain and its causal units carry more masked tiles).
+  if (cta_pair_mode() == 1) {
+    const int max_pairs = prefill_max_pairs();
+    if (max_pairs < 1) { delete p; return MLA_ERR_CUDA; }
+    rc = build_plan(qo_indptr, kv_indptr, batch, num_heads, causal != 0, window_left, max_pairs, &p->plan,
+                    2 * kTileM);
+    if (rc != MLA_OK) { delete p; return rc; }
+    p->pair = 1;
+  }
   cudaGetDevice(&p->device);
   p->batch = batch;
   p->num_heads = num_heads;
@@ -184,6 +198,9 @@ static int prefill_run_impl(mla_plan_t p, const void* q, const void* k, const vo
   const uint64_t kv_rows = p->total_kv > 0 ? (uint64_t)p->total_kv : 1;
   CUtensorMap tq, tk, tv, tr;
   const uint32_t box[3] = {64, 1, 128};
+  // A CTA of a pair loads 64 keys of each K tile.
+  const uint32_t krows = p->pair ? 64 : 128;
+  const uint32_t kbox[3] = {64, 1, krows};
   {
     const uint64_t dims[3] = {192, H, (uint64_t)p->total_q};
     const uint64_t strides[2] = {192 * 2, H * 192 * 2};
@@ -193,12 +210,12 @@ static int prefill_run_impl(mla_plan_t p, const void* q, const void* k, const vo
     const uint64_t kd = shared_rope ? 128 : 192;
     const uint64_t dims[3] = {kd, H, kv_rows};
     const uint64_t strides[2] = {kd * 2, H * kd * 2};
-    if (make_tensor_map_bf16(&tk, kb, 3, dims, strides, box) != MLA_OK) return MLA_ERR_CUDA;
+    if (make_tensor_map_bf16(&tk, kb, 3, dims, strides, kbox) != MLA_OK) return MLA_ERR_CUDA;
   }
   if (shared_rope && p->total_kv > 0) {
     const uint64_t dims[2] = {64, kv_rows};
     const uint64_t strides[1] = {(uint64_t)rope_stride * 2};
-    const uint32_t rbox[2] = {64, 128};
+    const uint32_t rbox[2] = {64, krows};
     if (make_tensor_map_bf16(&tr, k_rope, 2, dims, strides, rbox) != MLA_OK) return MLA_ERR_CUDA;
   } else {
     tr = tk;
@@ -228,6 +245,7 @@ static int prefill_run_impl(mla_plan_t p, const void* q, const void* k, const vo
   prm.force_timeout = p->forced_timeout_ns != 0;
   prm.wait_limit_ns = prm.force_timeout ? p->forced_timeout_ns : kWaitLimitNs;
   prm.shared_rope = shared_rope && p->total_kv > 0;
+  prm.pair = p->pair;
   const cudaStream_t s = as_stream(stream);
   if (launch_prefill(tq, tk, tv, tr, prm, p->num_ctas, s) != cudaSuccess) return MLA_ERR_CUDA;
   // Remember the last use for mla_plan_destroy.  A run captured into a graph is not
@@ -293,6 +311,7 @@ int mla_plan_query(mla_plan_t p, int which, int64_t* value) {
     case 3: *value = p->total_kv; break;
     case 4: *value = p->plan.allowed_pairs; break;
     case 5: *value = p->plan.kv_tiles; break;
+    case 6: *value = p->pair; break;
     default: return MLA_ERR_INVALID_ARG;
   }
   return MLA_OK;

@@ -136,6 +136,7 @@ extern "C" MLA_API int mla_prefill_run_noalloc(const int32_t* qo_indptr, const i
   prm.cap_ex2_scale = 2.f * LOG2E * prm.x_to_cap;
   prm.force_timeout = 0;
   prm.shared_rope = 0;
+  prm.pair = 0;
   prm.wait_limit_ns = kWaitLimitNs;
   const int num_ctas = (int)plan.cta_offsets.size() - 1;
   return launch_prefill(tq, tk, tv, tk, prm, num_ctas, s) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;

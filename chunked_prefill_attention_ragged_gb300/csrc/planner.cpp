@@ -44,8 +44,9 @@ int64_t allowed_pairs(int64_t lq, int64_t lkv, bool causal, int window_left) {
 }  // namespace
 
 int build_plan(const int32_t* qo, const int32_t* kv, int batch, int num_heads, bool causal,
-               int window_left, int max_ctas, PlanResult* out) {
+               int window_left, int max_ctas, PlanResult* out, int rows_per_unit) {
   if (!qo || !kv || !out || batch < 0 || num_heads < 1 || max_ctas < 1) return MLA_ERR_INVALID_ARG;
+  if (rows_per_unit != kTileM && rows_per_unit != 2 * kTileM) return MLA_ERR_INVALID_ARG;
   if (window_left < -1) return MLA_ERR_INVALID_ARG;
   if (qo[0] != 0 || kv[0] != 0) return MLA_ERR_SHAPE;
   for (int r = 0; r < batch; ++r)
@@ -72,8 +73,8 @@ int build_plan(const int32_t* qo, const int32_t* kv, int batch, int num_heads, b
     const int64_t diag = lkv - lq;
     // Tiles of this request, identical for every head.
     std::vector<std::pair<Unit, int64_t>> tiles;
-    for (int64_t p0 = 0; p0 < lq; p0 += kTileM) {
-      const int64_t p1 = std::min(lq, p0 + kTileM) - 1;
+    for (int64_t p0 = 0; p0 < lq; p0 += rows_per_unit) {
+      const int64_t p1 = std::min(lq, p0 + rows_per_unit) - 1;
       int64_t lo, hi;
       key_span(p0, p1, lkv, diag, causal, window_left, &lo, &hi);
       int32_t tlo = 0, thi = 0;   // empty range: the kernel writes O = 0, LSE = -inf

@@ -33,8 +33,11 @@ struct PlanResult {
   int64_t kv_tiles = 0;           // sum over units of (hi - lo)
 };
 
-// Returns 0 or a negative MLA_ERR_* code.  Inputs are validated here.
+// Returns 0 or a negative MLA_ERR_* code.  Inputs are validated here.  rows_per_unit is
+// kTileM (one CTA per unit) or 2 * kTileM (a CTA pair per unit: the two CTAs of a cluster
+// take the unit's first and second 128 rows and share its key tiles); max_ctas then
+// counts CTA pairs.
 int build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr, int batch, int num_heads,
-               bool causal, int window_left, int max_ctas, PlanResult* out);
+               bool causal, int window_left, int max_ctas, PlanResult* out, int rows_per_unit = kTileM);
 
 }  // namespace mla

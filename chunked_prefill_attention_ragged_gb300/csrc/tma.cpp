@@ -52,6 +52,14 @@ uint64_t forced_timeout_ns() {
   return (uint64_t)x;
 }
 
+int cta_pair_mode() {
+  const char* v = std::getenv("MLA_PLAN_CTA_PAIRS");
+  if (!v || !*v) return -1;
+  if (v[0] == '0' && v[1] == '\0') return 0;
+  if (v[0] == '1' && v[1] == '\0') return 1;
+  return -1;
+}
+
 int device_sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;

@@ -176,9 +176,11 @@ MLA_API int mla_prefill_status(mla_plan_t plan);
  */
 MLA_API int mla_plan_destroy(mla_plan_t plan);
 
-/* Plan facts: which = 0 work units, 1 CTAs launched, 2 total query rows,
- * 3 total key rows, 4 allowed (query, key) pairs summed over requests (one head),
- * 5 KV tiles summed over units. */
+/* Plan facts: which = 0 work units, 1 CTAs launched (CTA pairs when 6 is 1), 2 total
+ * query rows, 3 total key rows, 4 allowed (query, key) pairs summed over requests (one
+ * head), 5 KV tiles summed over units, 6 whether units of 256 query rows run on clusters
+ * of two CTAs (1) or units of 128 rows on single CTAs (0).  Single CTAs unless the
+ * environment variable MLA_PLAN_CTA_PAIRS is "1" when the plan is made. */
 MLA_API int mla_plan_query(mla_plan_t plan, int which, int64_t* value);
 
 /*
@@ -188,7 +190,9 @@ MLA_API int mla_plan_query(mla_plan_t plan, int which, int64_t* value);
  *   {head, q_row0, q_rows, q_pos0, kv_row0, kv_len, diag, kv_tile_lo | kv_tile_hi << 16}
  * in execution order, and cta_offsets[num_ctas+1] (CTA c runs units
  * [cta_offsets[c], cta_offsets[c+1])).  *num_units receives the count even
- * when capacity is too small (then MLA_ERR_SHAPE is returned).
+ * when capacity is too small (then MLA_ERR_SHAPE is returned).  With
+ * MLA_PLAN_CTA_PAIRS = "1" units are 256 query rows (q_rows up to 256) and num_ctas
+ * counts CTA pairs, as mla_prefill_plan then plans.
  */
 MLA_API int mla_plan_units_host(const int32_t* qo_indptr, const int32_t* kv_indptr, int batch,
                         int num_heads, int causal, int window_left, int num_ctas,

@@ -82,8 +82,9 @@ def test_entry_points_reject_null_and_misaligned():
     assert lib.mla_cache_write(16, 4, 64, 576, 32, 12, 8, None, None) == -1   # misaligned slot_mapping
 
 
-def _coverage(units, qo, kv, heads, causal, window):
-    """For every (head, request, row, key): how many units cover it, and unit validity."""
+def _coverage(units, qo, kv, heads, causal, window, rows=128):
+    """For every (head, request, row, key): how many units cover it, and unit validity
+    (units of `rows` query rows)."""
     B = len(qo) - 1
     cover = {}
     for u in units:
@@ -92,7 +93,7 @@ def _coverage(units, qo, kv, heads, causal, window):
         r = int(np.searchsorted(qo, q_row0, side="right") - 1)
         assert qo[r] + q_pos0 == q_row0 and kv_row0 == kv[r] and kv_len == kv[r + 1] - kv[r]
         lq = qo[r + 1] - qo[r]
-        assert diag == kv_len - lq and 1 <= q_rows <= 128 and q_pos0 + q_rows <= lq and q_pos0 % 128 == 0
+        assert diag == kv_len - lq and 1 <= q_rows <= rows and q_pos0 + q_rows <= lq and q_pos0 % rows == 0
         m = allowed_mask(lq, kv_len, causal, window, np.arange(q_pos0, q_pos0 + q_rows))
         for t in range(lo, hi):   # no kv tile in the range is fully masked
             assert m[:, t * 128:(t + 1) * 128].any()
@@ -104,10 +105,10 @@ def _coverage(units, qo, kv, heads, causal, window):
             lq = qo[r + 1] - qo[r]
             lkv = kv[r + 1] - kv[r]
             full = allowed_mask(lq, lkv, causal, window)
-            for p0 in range(0, lq, 128):
+            for p0 in range(0, lq, rows):
                 lo, hi, m = cover.pop((h, r, p0))
                 # every allowed key of these rows lies inside the unit's tile range
-                allowed_cols = np.nonzero(full[p0:p0 + 128].any(axis=0))[0]
+                allowed_cols = np.nonzero(full[p0:p0 + rows].any(axis=0))[0]
                 if allowed_cols.size:
                     assert allowed_cols.min() >= lo * 128 and allowed_cols.max() < hi * 128
                 else:
@@ -134,6 +135,18 @@ def test_planner_covers_every_allowed_pair_once(qlens, kvlens, heads, causal, wi
         units, offs = mla.mla_plan_units_host(qo, kv, heads, causal, window, ctas)
         assert offs[0] == 0 and offs[-1] == len(units) and np.all(np.diff(offs) >= 0)
         _coverage(units, qo, kv, heads, causal, window)
+
+
+@pytest.mark.parametrize("qlens,kvlens,heads,causal,window", PLAN_CASES)
+def test_pair_planner_covers_every_allowed_pair_once(monkeypatch, qlens, kvlens, heads, causal, window):
+    """With MLA_PLAN_CTA_PAIRS=1 units are 256 rows (one per CTA pair), same coverage rules."""
+    monkeypatch.setenv("MLA_PLAN_CTA_PAIRS", "1")
+    qo = wl.indptr_from_lengths(qlens)
+    kv = wl.indptr_from_lengths(kvlens if kvlens is not None else qlens)
+    for pairs in (1, 3, 76):
+        units, offs = mla.mla_plan_units_host(qo, kv, heads, causal, window, pairs)
+        assert offs[0] == 0 and offs[-1] == len(units) and np.all(np.diff(offs) >= 0)
+        _coverage(units, qo, kv, heads, causal, window, rows=256)
 
 
 def test_planner_balance_on_long_causal_request():
