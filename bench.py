@@ -849,6 +849,16 @@ def kernel_case(name: str, reps: int = 3):
         v = torch.empty(4096, 128, 128, dtype=torch.bfloat16, device=dev)
         for _ in range(reps):
             mla.mla_up_proj_paged(cache, table, cu, st, 4096, w, 128, k, v)
+    elif name == "up_proj_paged_split":
+        # the same rows, decompressed as the pipeline does: K_nope [T, H, 128] + one rope row per token
+        cache, w = dev_bf16(cb.cache), dev_bf16(cb.w_kvb)
+        cu = torch.tensor([0, 1024, 2048, 3072, 4096], dtype=torch.int32, device=dev)
+        st = torch.zeros(4, dtype=torch.int32, device=dev)
+        k = torch.empty(4096, 128, 128, dtype=torch.bfloat16, device=dev)
+        v = torch.empty(4096, 128, 128, dtype=torch.bfloat16, device=dev)
+        rope = torch.empty(4096, 64, dtype=torch.bfloat16, device=dev)
+        for _ in range(reps):
+            mla.mla_up_proj_paged_split(cache, table, cu, st, 4096, w, 128, k, v, rope)
     else:
         raise ValueError(name)
     torch.cuda.synchronize()
@@ -866,7 +876,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-chunked", action="store_true")
     ap.add_argument("--no-workloads", action="store_true", help="skip the rows of the other workloads")
-    ap.add_argument("--kernel-case", choices=["fp8_gather", "up_proj_paged"], default=None,
+    ap.add_argument("--kernel-case", choices=["fp8_gather", "up_proj_paged", "up_proj_paged_split"], default=None,
                     help="launch one kernel on a small case and exit (for profiler captures)")
     args = ap.parse_args()
     if args.kernel_case:
