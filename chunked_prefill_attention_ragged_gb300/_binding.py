@@ -50,6 +50,9 @@ _SIGNATURES = {
     "mla_merge_state": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_int, _c_int, _c_vp]),
     "mla_prefill_run_noalloc": (_c_int, [_i32p, _i32p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_f, _c_int, _c_f,
                                          _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
+    "mla_absorbed_plan": (_c_int, [ctypes.POINTER(_c_vp), _i32p, _i32p, _c_int, _c_int, _c_int, _c_int, _c_f, _c_f,
+                                   _c_vp]),
+    "mla_absorbed_run": (_c_int, [_c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_int, _c_vp, _c_vp, _c_vp]),
 }
 EXPORTED = tuple(_SIGNATURES)
 
@@ -180,6 +183,66 @@ def mla_prefill_plan(qo_indptr, kv_indptr, num_heads: int, head_dim_qk: int = 19
                                       head_dim_vo, int(bool(causal)), float(sm_scale), int(window_left),
                                       float(logits_soft_cap), _stream(stream)), "mla_prefill_plan")
     return PrefillPlan(h, num_heads, int(qo[-1]), int(kv[-1]))
+
+
+class AbsorbedPlan(PrefillPlan):
+    """An ``mla_plan_t`` made by :func:`mla_absorbed_plan` (absorbed-weight MQA prefill over
+    the paged latent cache); status, query and destroy as for :class:`PrefillPlan`."""
+
+    def __init__(self, handle, num_heads: int, total_q: int, batch: int, block_size: int, max_kv_blocks: int):
+        super().__init__(handle, num_heads, total_q, 0)
+        self.batch = batch
+        self.block_size = block_size
+        self.max_kv_blocks = max_kv_blocks
+
+    def run(self, q_abs, cache, block_table, o=None, lse=None, return_lse=True, stream=None):
+        return mla_absorbed_run(self, q_abs, cache, block_table, o, lse, return_lse, stream)
+
+    def run_merge(self, *args, **kwargs):
+        raise TypeError("an absorbed plan runs with mla_absorbed_run")
+
+
+def mla_absorbed_plan(qo_indptr, kv_lens, num_heads: int, block_size: int, causal: bool = True,
+                      sm_scale: float | None = None, logits_soft_cap: float = 0.0, stream=None) -> AbsorbedPlan:
+    """Plan an absorbed-weight prefill: request r has qo_indptr[r+1]-qo_indptr[r] new query
+    rows, the last ones of its kv_lens[r] cache positions.  ``sm_scale`` is required."""
+    if sm_scale is None:
+        raise ValueError("sm_scale must be given explicitly")
+    qo, kl = _host_i32(qo_indptr), _host_i32(kv_lens)
+    if qo.ndim != 1 or qo.size < 1 or kl.shape != (qo.size - 1,):
+        raise ValueError("qo_indptr must be 1-D [batch+1] and kv_lens [batch]")
+    h = ctypes.c_void_p()
+    _check(library().mla_absorbed_plan(ctypes.byref(h), _ptr(qo), _ptr(kl), qo.size - 1, num_heads, int(block_size),
+                                       int(bool(causal)), float(sm_scale), float(logits_soft_cap), _stream(stream)),
+           "mla_absorbed_plan")
+    max_blocks = int(max(((int(x) + block_size - 1) // block_size for x in kl), default=0))
+    return AbsorbedPlan(h, num_heads, int(qo[-1]), qo.size - 1, int(block_size), max_blocks)
+
+
+def mla_absorbed_run(plan: AbsorbedPlan, q_abs, cache, block_table, o=None, lse=None, return_lse=True, stream=None):
+    """Run an absorbed plan: q_abs [T, H, 576], cache [NB, BS, 576], block_table [B, M] int32
+    (device) -> (o_lat [T, H, 512], lse [T, H] or None)."""
+    import torch
+    H, T = plan.num_heads, plan.total_q
+    if tuple(q_abs.shape) != (T, H, 576):
+        raise ValueError(f"q_abs must be [{T}, {H}, 576], got {tuple(q_abs.shape)}")
+    if cache.dim() != 3 or cache.shape[1] != plan.block_size or cache.shape[2] != 576:
+        raise ValueError(f"cache must be [num_blocks, {plan.block_size}, 576], got {tuple(cache.shape)}")
+    if block_table.dim() != 2 or block_table.shape[0] != plan.batch or block_table.shape[1] < plan.max_kv_blocks:
+        raise ValueError(f"block_table must be [{plan.batch}, >= {plan.max_kv_blocks}], got {tuple(block_table.shape)}")
+    if o is None:
+        o = torch.empty((T, H, 512), dtype=torch.bfloat16, device=q_abs.device)
+    if return_lse and lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q_abs.device)
+    if tuple(o.shape) != (T, H, 512) or (lse is not None and tuple(lse.shape) != (T, H)):
+        raise ValueError("o/lse shapes do not match the plan")
+    bf = torch.bfloat16
+    _check(library().mla_absorbed_run(plan.handle, _dev(q_abs, bf, "q_abs"), _dev(cache, bf, "cache"),
+                                      int(cache.shape[0]), _dev(block_table, torch.int32, "block_table"),
+                                      int(block_table.shape[1]), _dev(o, bf, "o"),
+                                      _dev(lse, torch.float32, "lse"), _stream(stream)),
+           "mla_absorbed_run")
+    return o, lse
 
 
 def mla_prefill_run(plan: PrefillPlan, q, k, v, o=None, lse=None, return_lse=True, stream=None):

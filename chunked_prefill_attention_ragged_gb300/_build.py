@@ -32,6 +32,7 @@ SOURCES = [
     "up_proj_kernel.cu",
     "noalloc.cu",
     "fp8_gather_kernel.cu",
+    "absorbed_kernel.cu",
 ]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

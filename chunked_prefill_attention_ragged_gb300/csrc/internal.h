@@ -89,6 +89,28 @@ cudaError_t launch_merge(const void* o_a, const float* lse_a, const void* o_b, c
 
 int device_sm_count();
 
+
+struct AbsorbedParams {
+  const AbsUnit* units;
+  const int32_t* block_table;   // [batch, max_blocks]
+  int max_blocks, block_size;
+  int64_t num_blocks;
+  int32_t oob_row;              // a row coordinate past the cache: the copy fills it with zeros
+  int piece_rows;               // rows of one tile load of the block map (0: gather4 only)
+  __nv_bfloat16* o;             // [total_q, H, 512]
+  float* lse;                   // [total_q, H] or null
+  int* status;
+  int num_heads, causal, has_cap, force_timeout;
+  float scale_log2, cap_log2, cap_ex2_scale;
+  uint64_t wait_limit_ns;
+};
+
+// The absorbed prefill kernel, one CTA per unit.  tq: q_abs as [total_q * H, 576] rows, box
+// {64, 128}; tc: the cache as [num_blocks * block_size, 576] rows, box {64, 1} (gather4);
+// tb: the same rows with box {64, piece_rows} (any valid map when piece_rows is 0).
+cudaError_t launch_absorbed(const CUtensorMap& tq, const CUtensorMap& tc, const CUtensorMap& tb,
+                            const AbsorbedParams& p, int num_units, cudaStream_t stream);
+
 // MLA_PLAN_CTA_PAIRS: 1 when "1" (plan prefills on CTA pairs), 0 when "0", -1 otherwise.
 int cta_pair_mode();
 

@@ -19,9 +19,12 @@ struct mla_plan {
   PlanResult plan;
   int num_ctas = 0;              // CTAs, or CTA pairs when pair is set
   int pair = 0;                  // units of 256 rows, each run by a cluster of two CTAs
+  int kind = 0;                  // 0: MHA prefill (mla_prefill_plan); 1: absorbed (mla_absorbed_plan)
+  int block_size = 0, max_kv_blocks = 0;   // absorbed: cache block size, blocks the longest request needs
+  std::vector<AbsUnit> aunits;   // absorbed: the work units (one CTA each)
   void* workspace = nullptr;     // units | cta offsets | status word (stream-ordered allocation)
   cudaEvent_t last_use = nullptr;  // recorded after the upload and after every uncaptured run
-  Unit* d_units = nullptr;
+  Unit* d_units = nullptr;       // MHA units, or the absorbed units (AbsUnit, same size)
   int32_t* d_offsets = nullptr;
   int* d_status = nullptr;
 };
@@ -57,6 +60,40 @@ bool stream_capturing(cudaStream_t s) {
 void free_plan_storage(mla_plan* p) {
   if (p->last_use) cudaEventDestroy(p->last_use);
   delete p;
+}
+
+// The plan's device workspace (stream-ordered): work units, CTA offsets, status word; the
+// uploads are ordered on `s` and recorded as the plan's first use.  Frees the plan on error.
+int upload_plan(mla_plan* p, const void* units, size_t unit_bytes, const int32_t* offsets, size_t num_offsets,
+                cudaStream_t s) {
+  const size_t units_bytes = round_up(std::max<size_t>(1, unit_bytes), 256);
+  const size_t offs_bytes = round_up(std::max<size_t>(1, num_offsets) * sizeof(int32_t), 256);
+  if (cudaEventCreateWithFlags(&p->last_use, cudaEventDisableTiming) != cudaSuccess) {
+    p->last_use = nullptr;
+    free_plan_storage(p);
+    return MLA_ERR_CUDA;
+  }
+  if (cudaMallocAsync(&p->workspace, units_bytes + offs_bytes + 256, s) != cudaSuccess) {
+    free_plan_storage(p);
+    return MLA_ERR_CUDA;
+  }
+  char* ws = static_cast<char*>(p->workspace);
+  p->d_units = reinterpret_cast<Unit*>(ws);
+  p->d_offsets = reinterpret_cast<int32_t*>(ws + units_bytes);
+  p->d_status = reinterpret_cast<int*>(ws + units_bytes + offs_bytes);
+  cudaError_t e = cudaSuccess;
+  if (unit_bytes) e = cudaMemcpyAsync(p->d_units, units, unit_bytes, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && num_offsets)
+    e = cudaMemcpyAsync(p->d_offsets, offsets, num_offsets * sizeof(int32_t), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(p->d_status, 0, sizeof(int), s);
+  if (e == cudaSuccess) e = cudaEventRecord(p->last_use, s);
+  if (e != cudaSuccess) {
+    cudaStreamSynchronize(s);
+    cudaFreeAsync(p->workspace, s);
+    free_plan_storage(p);
+    return MLA_ERR_CUDA;
+  }
+  return MLA_OK;
 }
 
 }  // namespace
@@ -140,37 +177,9 @@ int mla_prefill_plan(mla_plan_t* out, const int32_t* qo_indptr, const int32_t* k
   p->total_kv = kv_indptr[batch];
   p->num_ctas = (int)p->plan.cta_offsets.size() - 1;
 
-  const size_t units_bytes = round_up(std::max<size_t>(1, p->plan.units.size()) * sizeof(Unit), 256);
-  const size_t offs_bytes = round_up(p->plan.cta_offsets.size() * sizeof(int32_t), 256);
-  cudaStream_t s = as_stream(stream);
-  if (cudaEventCreateWithFlags(&p->last_use, cudaEventDisableTiming) != cudaSuccess) {
-    p->last_use = nullptr;
-    free_plan_storage(p);
-    return MLA_ERR_CUDA;
-  }
-  if (cudaMallocAsync(&p->workspace, units_bytes + offs_bytes + 256, s) != cudaSuccess) {
-    free_plan_storage(p);
-    return MLA_ERR_CUDA;
-  }
-  char* ws = static_cast<char*>(p->workspace);
-  p->d_units = reinterpret_cast<Unit*>(ws);
-  p->d_offsets = reinterpret_cast<int32_t*>(ws + units_bytes);
-  p->d_status = reinterpret_cast<int*>(ws + units_bytes + offs_bytes);
-  cudaError_t e = cudaSuccess;
-  if (!p->plan.units.empty())
-    e = cudaMemcpyAsync(p->d_units, p->plan.units.data(), p->plan.units.size() * sizeof(Unit),
-                        cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(p->d_offsets, p->plan.cta_offsets.data(), p->plan.cta_offsets.size() * sizeof(int32_t),
-                        cudaMemcpyHostToDevice, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(p->d_status, 0, sizeof(int), s);
-  if (e == cudaSuccess) e = cudaEventRecord(p->last_use, s);
-  if (e != cudaSuccess) {
-    cudaStreamSynchronize(s);
-    cudaFreeAsync(p->workspace, s);
-    free_plan_storage(p);
-    return MLA_ERR_CUDA;
-  }
+  const int rc2 = upload_plan(p, p->plan.units.data(), p->plan.units.size() * sizeof(Unit), p->plan.cta_offsets.data(),
+                              p->plan.cta_offsets.size(), as_stream(stream));
+  if (rc2 != MLA_OK) return rc2;
   *out = p;
   return MLA_OK;
 }
@@ -180,7 +189,7 @@ int mla_prefill_plan(mla_plan_t* out, const int32_t* qo_indptr, const int32_t* k
 // heads.
 static int prefill_run_impl(mla_plan_t p, const void* q, const void* k, const void* k_rope, int64_t rope_stride,
                             const void* v, void* o, float* lse, int merge, void* stream) {
-  if (!p) return MLA_ERR_INVALID_ARG;
+  if (!p || p->kind != 0) return MLA_ERR_INVALID_ARG;
   if (merge && !lse) return MLA_ERR_INVALID_ARG;
   if (p->plan.units.empty()) return MLA_OK;   // no query rows
   if (!q || !o || !aligned16(q) || !aligned16(o) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
@@ -302,10 +311,113 @@ int mla_plan_destroy(mla_plan_t p) {
   return rc;
 }
 
+int mla_absorbed_plan(mla_plan_t* out, const int32_t* qo_indptr, const int32_t* kv_lens, int batch, int num_heads,
+                      int block_size, int causal, float sm_scale, float logits_soft_cap, void* stream) {
+  if (!out) return MLA_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!qo_indptr || !kv_lens || batch < 0 || num_heads < 1 || num_heads > 65535 || block_size < 1)
+    return MLA_ERR_INVALID_ARG;
+  if (!std::isfinite(sm_scale) || !(sm_scale > 0.f) || !std::isfinite(logits_soft_cap)) return MLA_ERR_INVALID_ARG;
+  std::vector<AbsUnit> units;
+  int64_t allowed = 0;
+  const int rc = build_absorbed_units(qo_indptr, kv_lens, batch, num_heads, causal != 0, &units, &allowed);
+  if (rc != MLA_OK) return rc;
+  int max_kv_blocks = 0;
+  for (int r = 0; r < batch; ++r)
+    max_kv_blocks = std::max(max_kv_blocks, (int)(((int64_t)kv_lens[r] + block_size - 1) / block_size));
+  mla_plan* p = new (std::nothrow) mla_plan();
+  if (!p) return MLA_ERR_CUDA;
+  cudaGetDevice(&p->device);
+  p->kind = 1;
+  p->batch = batch;
+  p->num_heads = num_heads;
+  p->causal = causal != 0;
+  p->sm_scale = sm_scale;
+  p->soft_cap = logits_soft_cap > 0.f ? logits_soft_cap : 0.f;
+  p->forced_timeout_ns = forced_timeout_ns();
+  p->total_q = qo_indptr[batch];
+  p->block_size = block_size;
+  p->max_kv_blocks = max_kv_blocks;
+  p->plan.allowed_pairs = allowed;
+  for (const AbsUnit& u : units) p->plan.kv_tiles += u.ntiles;
+  p->aunits = std::move(units);
+  p->num_ctas = (int)p->aunits.size();
+  const int rc2 = upload_plan(p, p->aunits.data(), p->aunits.size() * sizeof(AbsUnit), nullptr, 0, as_stream(stream));
+  if (rc2 != MLA_OK) return rc2;
+  *out = p;
+  return MLA_OK;
+}
+
+int mla_absorbed_run(mla_plan_t p, const void* q_abs, const void* cache, int64_t num_blocks,
+                     const int32_t* block_table, int max_blocks_per_req, void* o_lat, float* lse, void* stream) {
+  if (!p || p->kind != 1 || num_blocks < 0 || max_blocks_per_req < 0) return MLA_ERR_INVALID_ARG;
+  if (p->aunits.empty()) return MLA_OK;   // no query rows
+  if (max_blocks_per_req < p->max_kv_blocks) return MLA_ERR_SHAPE;
+  // Slots are TMA row coordinates (int32), and one past the last slot marks a missing row.
+  if (num_blocks * (int64_t)p->block_size >= 0x7fffffff) return MLA_ERR_UNSUPPORTED;
+  if (!q_abs || !o_lat || !aligned16(q_abs) || !aligned16(o_lat) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return MLA_ERR_INVALID_ARG;
+  const bool any_keys = p->max_kv_blocks > 0;
+  if (any_keys && (!cache || !block_table || !aligned16(cache) || num_blocks < 1)) return MLA_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != p->device) return MLA_ERR_INVALID_ARG;
+  CUtensorMap tq, tc;
+  {
+    const uint64_t dims[2] = {576, (uint64_t)p->total_q * (uint64_t)p->num_heads};
+    const uint64_t strides[1] = {576 * 2};
+    const uint32_t box[2] = {64, 128};
+    if (make_tensor_map_bf16(&tq, q_abs, 2, dims, strides, box) != MLA_OK) return MLA_ERR_CUDA;
+  }
+  {
+    // With no key at all no cache row is ever fetched; the map still needs a valid base.
+    const uint64_t slots = any_keys ? (uint64_t)num_blocks * (uint64_t)p->block_size : 1;
+    const uint64_t dims[2] = {576, slots};
+    const uint64_t strides[1] = {576 * 2};
+    const uint32_t box[2] = {64, 1};   // one row high: rows are fetched four at a time by gather4
+    if (make_tensor_map_bf16(&tc, any_keys ? cache : q_abs, 2, dims, strides, box) != MLA_OK) return MLA_ERR_CUDA;
+  }
+  // Whole 64-key tiles by tile loads of block pieces: a block size that is a multiple of 64
+  // (one 64-row piece) or 8, 16 or 32 (64 / block_size pieces, each a whole block; 8 rows
+  // keep each piece on the 128-byte swizzle's 1024-byte period).
+  const int bs = p->block_size;
+  const int piece_rows = (bs % 64 == 0) ? 64 : ((bs % 8 == 0 && 64 % bs == 0) ? bs : 0);
+  CUtensorMap tb = tc;
+  if (any_keys && piece_rows > 0) {
+    const uint64_t dims[2] = {576, (uint64_t)num_blocks * (uint64_t)bs};
+    const uint64_t strides[1] = {576 * 2};
+    const uint32_t box[2] = {64, (uint32_t)piece_rows};
+    if (make_tensor_map_bf16(&tb, cache, 2, dims, strides, box) != MLA_OK) return MLA_ERR_CUDA;
+  }
+  AbsorbedParams prm;
+  prm.units = reinterpret_cast<const AbsUnit*>(p->d_units);
+  prm.block_table = block_table;
+  prm.max_blocks = max_blocks_per_req;
+  prm.block_size = p->block_size;
+  prm.num_blocks = any_keys ? num_blocks : 0;
+  prm.oob_row = any_keys ? (int32_t)(num_blocks * p->block_size) : 1;
+  prm.piece_rows = any_keys ? piece_rows : 0;
+  prm.o = static_cast<__nv_bfloat16*>(o_lat);
+  prm.lse = lse;
+  prm.status = p->d_status;
+  prm.num_heads = p->num_heads;
+  prm.causal = p->causal;
+  const float LOG2E = 1.4426950408889634f;
+  prm.has_cap = p->soft_cap > 0.f;
+  prm.scale_log2 = p->sm_scale * LOG2E;
+  prm.cap_log2 = prm.has_cap ? p->soft_cap * LOG2E : 0.f;
+  prm.cap_ex2_scale = prm.has_cap ? 2.f * LOG2E * p->sm_scale / p->soft_cap : 0.f;
+  prm.force_timeout = p->forced_timeout_ns != 0;
+  prm.wait_limit_ns = prm.force_timeout ? p->forced_timeout_ns : kWaitLimitNs;
+  const cudaStream_t s = as_stream(stream);
+  if (launch_absorbed(tq, tc, tb, prm, (int)p->aunits.size(), s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (!stream_capturing(s) && cudaEventRecord(p->last_use, s) != cudaSuccess) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
 int mla_plan_query(mla_plan_t p, int which, int64_t* value) {
   if (!p || !value) return MLA_ERR_INVALID_ARG;
   switch (which) {
-    case 0: *value = (int64_t)p->plan.units.size(); break;
+    case 0: *value = p->kind ? (int64_t)p->aunits.size() : (int64_t)p->plan.units.size(); break;
     case 1: *value = p->num_ctas; break;
     case 2: *value = p->total_q; break;
     case 3: *value = p->total_kv; break;

@@ -7,6 +7,7 @@
 #include "planner.h"
 
 #include <algorithm>
+#include <climits>
 #include <functional>
 #include <queue>
 #include <utility>
@@ -146,6 +147,45 @@ int build_plan(const int32_t* qo, const int32_t* kv, int batch, int num_heads, b
     for (int32_t i : per_cta[c]) out->units.push_back(pending[i]);
   }
   out->cta_offsets[num_ctas] = (int32_t)out->units.size();
+  return MLA_OK;
+}
+
+int build_absorbed_units(const int32_t* qo, const int32_t* kv_lens, int batch, int num_heads, bool causal,
+                         std::vector<AbsUnit>* out, int64_t* allowed) {
+  if (!qo || !kv_lens || !out || !allowed || batch < 0 || num_heads < 1) return MLA_ERR_INVALID_ARG;
+  if (qo[0] != 0) return MLA_ERR_SHAPE;
+  for (int r = 0; r < batch; ++r)
+    if (qo[r + 1] < qo[r] || kv_lens[r] < 0) return MLA_ERR_SHAPE;
+  // Pair indices (row * heads + head) and key positions are 32-bit on the device.
+  if ((int64_t)qo[batch] * num_heads > INT32_MAX - 128) return MLA_ERR_UNSUPPORTED;
+  out->clear();
+  *allowed = 0;
+  constexpr int kPairs = 128, kKeys = 64;
+  for (int r = 0; r < batch; ++r) {
+    const int64_t lq = qo[r + 1] - qo[r], lkv = kv_lens[r];
+    if (lq == 0) continue;
+    *allowed += allowed_pairs(lq, lkv, causal, -1);
+    const int64_t diag = lkv - lq, pairs = lq * num_heads;
+    for (int64_t p0 = 0; p0 < pairs; p0 += kPairs) {
+      const int64_t np = std::min<int64_t>(kPairs, pairs - p0);
+      const int64_t last_pos = (p0 + np - 1) / num_heads;   // position of the run's last row
+      int64_t khi = causal ? std::min(lkv, last_pos + diag + 1) : lkv;
+      if (khi < 0) khi = 0;
+      AbsUnit u;
+      u.pair0 = (int32_t)((int64_t)qo[r] * num_heads + p0);
+      u.npairs = (int32_t)np;
+      u.q_row0 = qo[r];
+      u.q_len = (int32_t)lq;
+      u.kv_len = (int32_t)lkv;
+      u.ntiles = (int32_t)((khi + kKeys - 1) / kKeys);
+      u.req = r;
+      for (int h = 0; h < 2; ++h) {
+        u.half = h;
+        out->push_back(u);
+      }
+    }
+  }
+  std::stable_sort(out->begin(), out->end(), [](const AbsUnit& a, const AbsUnit& b) { return a.ntiles > b.ntiles; });
   return MLA_OK;
 }
 

@@ -40,4 +40,28 @@ struct PlanResult {
 int build_plan(const int32_t* qo_indptr, const int32_t* kv_indptr, int batch, int num_heads,
                bool causal, int window_left, int max_ctas, PlanResult* out, int rows_per_unit = kTileM);
 
+// One unit of the absorbed-weight (MQA) prefill: up to 128 consecutive (query row, head)
+// pairs of one request and one half of the 512 latent value columns.  32 bytes, read by
+// the kernel.
+struct AbsUnit {
+  int32_t pair0;    // first pair: global query row * num_heads + head
+  int32_t npairs;   // pairs in the unit (1..128)
+  int32_t q_row0;   // global row of the request's first query
+  int32_t q_len;    // queries of the request
+  int32_t kv_len;   // keys of the request (its cache positions 0 .. kv_len - 1)
+  int32_t ntiles;   // 64-key tiles holding an allowed key of some pair of the unit
+  int32_t half;     // value columns [256 half, 256 half + 256)
+  int32_t req;      // request (block-table row)
+};
+static_assert(sizeof(AbsUnit) == 32, "absorbed unit layout");
+
+// Units of the absorbed-weight prefill: for each request r (queries qo[r] .. qo[r+1] - 1,
+// the last q_len of its kv_lens[r] cache positions), its (row, head) pairs in runs of 128,
+// each run once per value half, with the number of 64-key tiles that hold an allowed key
+// of the run's last pair (the one with the most keys); longest first.  *allowed_pairs
+// receives the allowed (query, key) pairs summed over requests (one head).  Returns 0 or a
+// negative MLA_ERR_* code.
+int build_absorbed_units(const int32_t* qo_indptr, const int32_t* kv_lens, int batch, int num_heads, bool causal,
+                         std::vector<AbsUnit>* out, int64_t* allowed_pairs);
+
 }  // namespace mla

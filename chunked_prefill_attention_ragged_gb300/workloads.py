@@ -270,3 +270,60 @@ def make_chunked_prefix() -> ChunkedPrefixBatch:
     lens = workload_lengths(2, rng)
     return random_chunked_prefix(0, lens, np.full(4, 8192), WORKLOAD_HEADS[2], num_blocks=1024,
                                  block_size=64, chunk_tokens=4096, name=WORKLOAD_NAMES[2], rng=rng)
+
+
+@dataclass
+class AbsorbedBatch:
+    """Absorbed-weight prefill inputs: request r has q_lens[r] new query rows, the last of
+    its kv_lens[r] positions in the paged latent cache.
+
+    q_abs: [sum q_lens, H, 576] bf16 bits (the absorbed query W_UK(h) q_nope(h) || q_rope(h),
+    drawn directly), cache: [num_blocks, block_size, 576] bf16 bits, block_table: int32
+    [B, max blocks] (unused entries -1)."""
+    name: str
+    q_lens: np.ndarray
+    kv_lens: np.ndarray
+    num_heads: int
+    block_size: int
+    causal: bool
+    sm_scale: float
+    logits_soft_cap: float
+    q_abs: np.ndarray
+    cache: np.ndarray
+    block_table: np.ndarray
+    qo_indptr: np.ndarray = field(init=False)
+
+    def __post_init__(self):
+        self.qo_indptr = indptr_from_lengths(self.q_lens)
+
+    @property
+    def batch(self) -> int:
+        return len(self.q_lens)
+
+
+def random_absorbed(seed: int, q_lens, kv_lens, num_heads: int, *, block_size: int = 64,
+                    num_blocks: int | None = None, causal: bool = True, logits_soft_cap: float = 0.0,
+                    sm_scale: float = DEFAULT_SM_SCALE, name: str = "absorbed") -> AbsorbedBatch:
+    """Draw an absorbed-weight prefill problem (same recipe: N(0,1) rounded to bf16).
+
+    The block table is the first sum(ceil(kv_len/block_size)) entries of a random
+    permutation of the cache blocks, handed out request by request; the cache is filled
+    everywhere, so a wrong block index reads visible values.  The softmax scale is the MHA
+    one (192^-0.5) unless given."""
+    rng = np.random.default_rng(seed)
+    q_lens = np.asarray(q_lens, dtype=np.int64)
+    kv_lens = np.asarray(kv_lens, dtype=np.int64)
+    per_req = [-(-int(k) // block_size) for k in kv_lens]
+    if num_blocks is None:
+        num_blocks = max(1, sum(per_req) + 3)
+    assert sum(per_req) <= num_blocks
+    q_abs = _normal_bf16(rng, (int(q_lens.sum()), num_heads, LATENT_DIM))
+    cache = _normal_bf16(rng, (num_blocks, block_size, LATENT_DIM))
+    perm = rng.permutation(num_blocks).astype(np.int32)
+    table = np.full((len(q_lens), max(1, max(per_req, default=1))), -1, dtype=np.int32)
+    pos = 0
+    for r, nb in enumerate(per_req):
+        table[r, :nb] = perm[pos:pos + nb]
+        pos += nb
+    return AbsorbedBatch(name, q_lens, kv_lens, num_heads, block_size, causal, float(sm_scale),
+                         float(logits_soft_cap), q_abs, cache, table)

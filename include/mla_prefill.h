@@ -325,6 +325,48 @@ MLA_API int mla_up_proj_paged_split(const void* cache, int64_t num_blocks, int b
                                     void* stream);
 
 /* ======================================================================
+ * Absorbed-weight paged prefill.  [sglang] prefill with a cached prefix runs
+ * forward_absorb: every head attends to the compressed cache rows themselves
+ * (multi-query attention, one KV head: Dqk = 576 = 512 latent + 64 rope, Dv =
+ * 512), with W_UK folded into the query; [TVM] sm_scale is explicit because
+ * absorption changes the effective head dim; [vLLM-V4] slot rule for the
+ * cache positions.
+ * ====================================================================== */
+/*
+ * Plan (host work list + device workspace) for a batch:
+ *   qo_indptr : HOST int32 [batch+1], new query rows per request (qo[0] = 0)
+ *   kv_lens   : HOST int32 [batch], keys per request: its cache positions
+ *               0 .. kv_lens[r]-1 (the new tokens' rows must already be in the
+ *               cache); query row i of a request of q_len rows sits at position
+ *               kv_len - q_len + i (bottom-right causal alignment; rows with no
+ *               allowed key get O = 0, LSE = -inf)
+ *   block_size: cache block size (any value >= 1)
+ *   causal, sm_scale (> 0), logits_soft_cap (<= 0: none) as for mla_prefill_plan
+ * The plan object is an mla_plan_t: mla_prefill_status, mla_plan_query and
+ * mla_plan_destroy apply to it; mla_prefill_run and its variants reject it
+ * (MLA_ERR_INVALID_ARG), as mla_absorbed_run rejects an MHA plan.
+ */
+MLA_API int mla_absorbed_plan(mla_plan_t* out, const int32_t* qo_indptr, const int32_t* kv_lens, int batch,
+                              int num_heads, int block_size, int causal, float sm_scale, float logits_soft_cap,
+                              void* stream);
+
+/*
+ *   q_abs      : bf16 [total_q, num_heads, 576] (W_UK(h) q_nope(h) || q_rope(h))
+ *   cache      : bf16 [num_blocks, block_size, 576] (512 latent + 64 rope per slot)
+ *   block_table: DEVICE int32 [batch, max_blocks_per_req]; max_blocks_per_req must
+ *                cover the longest request (MLA_ERR_SHAPE otherwise)
+ *   o_lat      : bf16 [total_q, num_heads, 512] (O_lat; the MHA output of head h
+ *                is O_lat(h) W_UV(h))
+ *   lse        : fp32 [total_q, num_heads] natural-log LSE, or NULL
+ * A block id outside [0, num_blocks) reads as a zero row and sets
+ * MLA_DEVSTAT_BAD_INDEX in the plan's status word (mla_prefill_status then
+ * returns MLA_ERR_DEVICE_BOUNDS).  Allocates nothing.
+ */
+MLA_API int mla_absorbed_run(mla_plan_t plan, const void* q_abs, const void* cache, int64_t num_blocks,
+                             const int32_t* block_table, int max_blocks_per_req, void* o_lat, float* lse,
+                             void* stream);
+
+/* ======================================================================
  * LSE merge of two partial attention states.  [vLLM-FI]
  * run_prefill_context_chunk always returns LSE so chunk results can merge.
  * ====================================================================== */

@@ -235,3 +235,31 @@ def test_shared_rope_binding_checks_shapes():
                                              torch.zeros(20, 64, dtype=bf), v)
     with pytest.raises(ValueError):   # merge without the partial state
         _binding.mla_prefill_run_shared_rope(FakePlan(), q, kn, torch.zeros(20, 64, dtype=bf), v, merge=True)
+
+
+def test_absorbed_entry_points_check_arguments_on_the_host():
+    """Bad arguments to the absorbed-weight plan and run are refused before anything
+    touches the device (no GPU here)."""
+    import ctypes
+    lib = mla.library()
+    qo = np.array([0, 4, 9], dtype=np.int32)
+    kl = np.array([10, 9], dtype=np.int32)
+    P32 = ctypes.POINTER(ctypes.c_int32)
+    h = ctypes.c_void_p()
+
+    def plan(qo_, kl_, batch, heads, bs, scale, cap=0.0):
+        return lib.mla_absorbed_plan(ctypes.byref(h), qo_.ctypes.data_as(P32), kl_.ctypes.data_as(P32), batch,
+                                     heads, bs, 1, scale, cap, None)
+
+    assert plan(qo, kl, 2, 4, 0, 0.1) == -1                  # block size 0
+    assert plan(qo, kl, 2, 0, 64, 0.1) == -1                 # no heads
+    assert plan(qo, kl, 2, 4, 64, 0.0) == -1                 # sm_scale must be > 0
+    assert plan(qo, kl, 2, 4, 64, float("nan")) == -1
+    assert plan(np.array([1, 4, 9], dtype=np.int32), kl, 2, 4, 64, 0.1) == -2    # qo_indptr[0] != 0
+    assert plan(np.array([0, 4, 3], dtype=np.int32), kl, 2, 4, 64, 0.1) == -2    # not monotone
+    assert plan(qo, np.array([10, -1], dtype=np.int32), 2, 4, 64, 0.1) == -2     # negative kv length
+    assert lib.mla_absorbed_run(None, None, None, 0, None, 0, None, None, None) == -1
+    with pytest.raises(ValueError):
+        mla.mla_absorbed_plan(qo, kl, 4, 64)                  # sm_scale is required
+    with pytest.raises(ValueError):
+        mla.mla_absorbed_plan(qo, kl[:1], 4, 64, sm_scale=0.1)   # kv_lens must be [batch]
