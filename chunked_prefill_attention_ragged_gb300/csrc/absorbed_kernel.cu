@@ -21,7 +21,8 @@
 // five panels outside the value half (their slots refill for tile t + 1 at once), then
 // P(t - 1) V(t - 1) (which frees the value panels for tile t's loads), then the S
 // products over the value panels.
-//   warp 0     producer: the Q tile with tile loads; a 64-key tile of cache rows with
+//   warps 0, 3 producers (warp 0: the Q tile and the five panels outside the value half,
+//              warp 3: the four value panels): the Q tile with tile loads; cache rows with
 //              one tile load per panel and block piece when the block size lines up with
 //              the tile (a multiple of 64, or 8..32 dividing 64) and the tile lies inside
 //              kv_len; otherwise (a request's last tile, other block sizes) with
@@ -122,10 +123,14 @@ __device__ __forceinline__ int32_t key_row(const AbsorbedParams& p, const AbsUni
 }
 
 // ------------------------------------------------------------------ producer (warp 0)
+// Panels i0 .. i1 - 1 of the issue order of every tile (and the Q tile when i0 is 0): warp
+// 0 loads the five panels outside the value half, warp 3 the four value panels, so that
+// tile t + 1's first panels load as soon as S(t) has used their slots, without waiting
+// behind tile t's value panels (which wait for P(t - 1) V).
 __device__ void run_producer(const ACtx& c, const AbsorbedParams& p, const AbsUnit& u, const CUtensorMap* tq,
-                             const CUtensorMap* tc, const CUtensorMap* tb) {
+                             const CUtensorMap* tc, const CUtensorMap* tb, int i0, int i1) {
   const int lane = threadIdx.x & 31;
-  if (lane == 0) {
+  if (i0 == 0 && lane == 0) {
     mbar_arrive_expect_tx(c.bar(QF), NP * Q_PANEL);
     for (int i = 0; i < NP; ++i) tma_load_2d(c.sbase + OFF_Q + i * Q_PANEL, tq, c.bar(QF), i * 64, u.pair0);
   }
@@ -135,14 +140,18 @@ __device__ void run_producer(const ACtx& c, const AbsorbedParams& p, const AbsUn
   for (int i = 0; i < NP; ++i) issued[i] = 0;
   const int pieces = p.piece_rows > 0 ? AN / p.piece_rows : 0;
   for (int t = 0; t < u.ntiles && ok; ++t) {
-    // Whole tile inside the request and block pieces available: tile loads.
+    // Whole tile inside the request and block pieces available: tile loads, lane k
+    // holding piece k's row.  Rows are looked up once per tile, for all nine panels.
     const bool by_block = pieces > 0 && (t + 1) * AN <= u.kv_len;
     int32_t r4[4] = {0, 0, 0, 0};
-    if (!by_block && lane < 16) {
+    int32_t piece_row = 0;
+    if (by_block) {
+      if (lane < pieces) piece_row = key_row(p, u, t * AN + lane * p.piece_rows);
+    } else if (lane < 16) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) r4[j] = key_row(p, u, t * AN + 4 * lane + j);
     }
-    for (int i = 0; i < NP; ++i) {
+    for (int i = i0; i < i1; ++i) {
       const int pnl = panel_order(i, u.half);
       int free = 1;
       if (lane == 0 && t > 0) free = c.wait(KE + pnl, (t - 1) & 1);
@@ -150,10 +159,9 @@ __device__ void run_producer(const ACtx& c, const AbsorbedParams& p, const AbsUn
       if (lane == 0) mbar_arrive_expect_tx(c.bar(KF + pnl), K_PANEL);
       __syncwarp();
       if (by_block) {
-        if (lane == 0)
-          for (int k = 0; k < pieces; ++k)
-            tma_load_2d(c.sbase + OFF_K + pnl * K_PANEL + k * p.piece_rows * 128, tb, c.bar(KF + pnl), pnl * 64,
-                        key_row(p, u, t * AN + k * p.piece_rows));
+        if (lane < pieces)
+          tma_load_2d(c.sbase + OFF_K + pnl * K_PANEL + lane * p.piece_rows * 128, tb, c.bar(KF + pnl), pnl * 64,
+                      piece_row);
       } else if (lane < 16) {
         tma_gather4(c.sbase + OFF_K + pnl * K_PANEL + lane * 4 * 128, tc, c.bar(KF + pnl), pnl * 64, r4[0], r4[1],
                     r4[2], r4[3]);
@@ -163,7 +171,7 @@ __device__ void run_producer(const ACtx& c, const AbsorbedParams& p, const AbsUn
   }
   // Let every copy started here land before the CTA can exit.
   if (lane == 0) {
-    c.drain(QF, 0);
+    if (i0 == 0) c.drain(QF, 0);
     for (int pnl = 0; pnl < NP; ++pnl)
       if (issued[pnl] > 0) c.drain(KF + pnl, (issued[pnl] - 1) & 1);
   }
@@ -391,7 +399,9 @@ absorbed_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   if (warp == 0) {
-    if (u.ntiles > 0) run_producer(c, p, u, &tm_q, &tm_c, &tm_b);
+    if (u.ntiles > 0) run_producer(c, p, u, &tm_q, &tm_c, &tm_b, 0, 5);
+  } else if (warp == 3) {
+    if (u.ntiles > 0) run_producer(c, p, u, &tm_q, &tm_c, &tm_b, 5, NP);
   } else if (warp == 1) {
     if (lane == 0) run_mma(c, p, u, tmem);
   } else if (warp >= 4) {
