@@ -502,6 +502,11 @@ def bench_ours(args, world, rank, local):
     if rank == 0 and not args.no_chunked:
         chunked = bench_chunked(args, dev, peaks)
 
+    # ---- absorbed-weight prefill over the chunked-prefix workload's shape, rank 0
+    absorbed = None
+    if rank == 0 and not args.no_absorbed:
+        absorbed = bench_absorbed(dev, peaks)
+
     # ---- the other workloads, one row each, rank 0
     rows = None
     if rank == 0 and not args.no_workloads:
@@ -551,9 +556,58 @@ def bench_ours(args, world, rank, local):
     }
     if chunked is not None:
         line["chunked_prefix"] = chunked
+    if absorbed is not None:
+        line["absorbed_prefill"] = absorbed
     if rows is not None:
         line["workloads"] = rows
     return line
+
+
+def absorbed_case(small: bool):
+    """The absorbed-weight prefill inputs: the chunked-prefix workload's shape (4 requests of
+    2048 new rows, each the last of 10240 cache positions, 128 heads, 64-slot blocks), or a
+    small case (1 request of 64 rows over 2048 positions) for profiler captures."""
+    if small:
+        return wl.random_absorbed(1201, [64], [2048], 128, block_size=64, num_blocks=64)
+    return wl.random_absorbed(1200, [2048] * 4, [10240] * 4, 128, block_size=64, num_blocks=1024)
+
+
+def bench_absorbed(dev, peaks, reps: int = 3):
+    """mla_absorbed_run on the chunked-prefix shape: every head attends to the 576-wide
+    cache rows (prefix and new tokens) through the block table."""
+    import torch
+    import chunked_prefill_attention_ragged_gb300 as mla
+    b = absorbed_case(False)
+    plan = mla.mla_absorbed_plan(b.qo_indptr, b.kv_lens, b.num_heads, b.block_size, causal=True, sm_scale=b.sm_scale)
+
+    def to_bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    q, cache, table = to_bf(b.q_abs), to_bf(b.cache), torch.from_numpy(b.block_table).to(dev)
+    o, lse = plan.run(q, cache, table)
+    plan.run(q, cache, table, o, lse)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        plan.run(q, cache, table, o, lse)
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    if plan.status() != 0:
+        raise RuntimeError("absorbed prefill reported a device problem")
+    ms = statistics.median(ts)
+    flop = float(plan.allowed_pairs) * b.num_heads * 2 * (576 + 512)
+    tf = flop / (ms * 1e-3) / 1e12
+    return {"workload": "absorbed_4x2048_over_10240_h128_bs64", "ms": round(ms, 3), "launches": reps,
+            "flop": flop, "tflops": round(tf, 1), "plan_units": plan.num_units,
+            "roofline": {"kernel": "absorbed_kernel", "bound": "tensor", "achieved": round(tf, 1),
+                         "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": round(tf / peaks["bf16_tflops"], 4)},
+            "note": "FLOPs counted as 2 x (576 + 512) per allowed (query, key) pair and head; each CTA "
+                    "computes S for its half of the 512 value columns (S work done twice)",
+            "l2": "inputs (2.4 GB of queries) larger than L2, no flush"}
 
 
 def bench_chunked(args, dev, peaks):
@@ -849,6 +903,15 @@ def kernel_case(name: str, reps: int = 3):
         v = torch.empty(4096, 128, 128, dtype=torch.bfloat16, device=dev)
         for _ in range(reps):
             mla.mla_up_proj_paged(cache, table, cu, st, 4096, w, 128, k, v)
+    elif name == "absorbed":
+        # 1 request of 64 new rows over 2048 cache positions, 128 heads (128 units)
+        b = absorbed_case(True)
+        plan = mla.mla_absorbed_plan(b.qo_indptr, b.kv_lens, b.num_heads, b.block_size, causal=True,
+                                     sm_scale=b.sm_scale)
+        q, cache = dev_bf16(b.q_abs), dev_bf16(b.cache)
+        tab = torch.from_numpy(b.block_table).to(dev)
+        for _ in range(reps):
+            plan.run(q, cache, tab)
     elif name == "up_proj_paged_split":
         # the same rows, decompressed as the pipeline does: K_nope [T, H, 128] + one rope row per token
         cache, w = dev_bf16(cb.cache), dev_bf16(cb.w_kvb)
@@ -876,7 +939,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-chunked", action="store_true")
     ap.add_argument("--no-workloads", action="store_true", help="skip the rows of the other workloads")
-    ap.add_argument("--kernel-case", choices=["fp8_gather", "up_proj_paged", "up_proj_paged_split"], default=None,
+    ap.add_argument("--no-absorbed", action="store_true", help="skip the absorbed-weight prefill row")
+    ap.add_argument("--kernel-case", choices=["fp8_gather", "up_proj_paged", "up_proj_paged_split", "absorbed"],
+                    default=None,
                     help="launch one kernel on a small case and exit (for profiler captures)")
     args = ap.parse_args()
     if args.kernel_case:
