@@ -56,9 +56,10 @@ constexpr int OFF_K = OFF_Q + NP * Q_PANEL;
 constexpr int OFF_BAR = OFF_K + NP * K_PANEL;
 enum ABar {
   QF = 0,             // Q tile landed
-  KF = 1,             // [panel slot] this tile's panel landed
-  KE = KF + NP,       // [panel slot] the panel's last product done: the slot may refill
-  SF = KE + NP,       // [S buffer] S = Q K^T done
+  KF = 1,             // [panel group] this tile's panels landed (group 0: the five panels
+                      // outside the value half; group 1: the value half's four)
+  KE = KF + 2,        // [panel group] the group's last product done: its slots may refill
+  SF = KE + 2,        // [S buffer] S = Q K^T done
   SE = SF + 2,        // [S buffer] P V done reading its P
   PR = SE + 2,        // [S buffer] P written by all four softmax warps
   OD = PR + 2,        // [tile parity] O += P V done
@@ -122,26 +123,28 @@ __device__ __forceinline__ int32_t key_row(const AbsorbedParams& p, const AbsUni
   return (int32_t)((int64_t)blk * p.block_size + (key - bi * p.block_size));
 }
 
-// ------------------------------------------------------------------ producer (warp 0)
-// Panels i0 .. i1 - 1 of the issue order of every tile (and the Q tile when i0 is 0): warp
-// 0 loads the five panels outside the value half, warp 3 the four value panels, so that
-// tile t + 1's first panels load as soon as S(t) has used their slots, without waiting
-// behind tile t's value panels (which wait for P(t - 1) V).
+// ------------------------------------------------------------------ producers (warps 0, 3)
+// Panel group g of every tile (and, for group 0, the Q tile): warp 0 loads the five panels
+// outside the value half, warp 3 the four value panels, so that tile t + 1's first panels
+// load as soon as S(t) has used their slots, without waiting behind tile t's value panels
+// (which wait for P(t - 1) V).  A whole tile inside kv_len with 64-row block pieces takes
+// one copy per run of adjacent panels (a three-dimensional map over the cache rows: 64
+// columns, rows, nine 64-column groups).
 __device__ void run_producer(const ACtx& c, const AbsorbedParams& p, const AbsUnit& u, const CUtensorMap* tq,
-                             const CUtensorMap* tc, const CUtensorMap* tb, int i0, int i1) {
+                             const CUtensorMap* tc, const CUtensorMap* tb, const CUtensorMap* t4, int g) {
   const int lane = threadIdx.x & 31;
-  if (i0 == 0 && lane == 0) {
+  const int h = u.half;
+  const int i0 = g == 0 ? 0 : 5, i1 = g == 0 ? 5 : NP;
+  if (g == 0 && lane == 0) {
     mbar_arrive_expect_tx(c.bar(QF), NP * Q_PANEL);
     for (int i = 0; i < NP; ++i) tma_load_2d(c.sbase + OFF_Q + i * Q_PANEL, tq, c.bar(QF), i * 64, u.pair0);
   }
   bool ok = true;
-  int issued[NP];   // tiles whose panel was requested, per slot
-#pragma unroll
-  for (int i = 0; i < NP; ++i) issued[i] = 0;
+  int issued = 0;   // tiles requested
   const int pieces = p.piece_rows > 0 ? AN / p.piece_rows : 0;
   for (int t = 0; t < u.ntiles && ok; ++t) {
     // Whole tile inside the request and block pieces available: tile loads, lane k
-    // holding piece k's row.  Rows are looked up once per tile, for all nine panels.
+    // holding piece k's row.  Rows are looked up once per tile, for all the panels.
     const bool by_block = pieces > 0 && (t + 1) * AN <= u.kv_len;
     int32_t r4[4] = {0, 0, 0, 0};
     int32_t piece_row = 0;
@@ -151,29 +154,43 @@ __device__ void run_producer(const ACtx& c, const AbsorbedParams& p, const AbsUn
 #pragma unroll
       for (int j = 0; j < 4; ++j) r4[j] = key_row(p, u, t * AN + 4 * lane + j);
     }
-    for (int i = i0; i < i1; ++i) {
-      const int pnl = panel_order(i, u.half);
-      int free = 1;
-      if (lane == 0 && t > 0) free = c.wait(KE + pnl, (t - 1) & 1);
-      if (!__shfl_sync(0xffffffffu, free, 0)) { ok = false; break; }
-      if (lane == 0) mbar_arrive_expect_tx(c.bar(KF + pnl), K_PANEL);
-      __syncwarp();
-      if (by_block) {
-        if (lane < pieces)
-          tma_load_2d(c.sbase + OFF_K + pnl * K_PANEL + lane * p.piece_rows * 128, tb, c.bar(KF + pnl), pnl * 64,
-                      piece_row);
-      } else if (lane < 16) {
-        tma_gather4(c.sbase + OFF_K + pnl * K_PANEL + lane * 4 * 128, tc, c.bar(KF + pnl), pnl * 64, r4[0], r4[1],
-                    r4[2], r4[3]);
+    int free = 1;
+    if (lane == 0 && t > 0) free = c.wait(KE + g, (t - 1) & 1);
+    if (!__shfl_sync(0xffffffffu, free, 0)) { ok = false; break; }
+    if (lane == 0) mbar_arrive_expect_tx(c.bar(KF + g), (i1 - i0) * K_PANEL);
+    __syncwarp();
+    if (by_block && p.grouped) {
+      // Runs of adjacent panels: value half [4h, 4h+4); outside it, half 0: [4, 8) and 8,
+      // half 1: [0, 4) and 8.
+      if (lane == 0) {
+        const uint32_t bar = c.bar(KF + g);
+        if (g == 1) {
+          tma_load_3d(c.sbase + OFF_K + 4 * h * K_PANEL, t4, bar, 0, piece_row, 4 * h);
+        } else {
+          const int run0 = h == 0 ? 4 : 0;
+          tma_load_3d(c.sbase + OFF_K + run0 * K_PANEL, t4, bar, 0, piece_row, run0);
+          tma_load_2d(c.sbase + OFF_K + 8 * K_PANEL, tb, bar, 8 * 64, piece_row);
+        }
       }
-      ++issued[pnl];
+    } else {
+      for (int i = i0; i < i1; ++i) {
+        const int pnl = panel_order(i, h);
+        if (by_block) {
+          if (lane < pieces)
+            tma_load_2d(c.sbase + OFF_K + pnl * K_PANEL + lane * p.piece_rows * 128, tb, c.bar(KF + g), pnl * 64,
+                        piece_row);
+        } else if (lane < 16) {
+          tma_gather4(c.sbase + OFF_K + pnl * K_PANEL + lane * 4 * 128, tc, c.bar(KF + g), pnl * 64, r4[0], r4[1],
+                      r4[2], r4[3]);
+        }
+      }
     }
+    ++issued;
   }
   // Let every copy started here land before the CTA can exit.
   if (lane == 0) {
-    if (i0 == 0) c.drain(QF, 0);
-    for (int pnl = 0; pnl < NP; ++pnl)
-      if (issued[pnl] > 0) c.drain(KF + pnl, (issued[pnl] - 1) & 1);
+    if (g == 0) c.drain(QF, 0);
+    if (issued > 0) c.drain(KF + g, (issued - 1) & 1);
   }
 }
 
@@ -186,26 +203,26 @@ __device__ void run_mma(const ACtx& c, const AbsorbedParams& p, const AbsUnit& u
   const uint64_t q_desc = sdesc_sw128(c.sbase + OFF_Q, 16, 1024);
   const uint64_t k_desc = sdesc_sw128(c.sbase + OFF_K, 16, 1024);
   const uint64_t v_desc = sdesc_sw128(c.sbase + OFF_K + 4 * h * K_PANEL, K_PANEL, 1024);
-  auto s_products = [&](int t, int i0, int i1) {   // S(t) += Q K^T over panels i0 .. i1 - 1 of the order
-    for (int i = i0; i < i1; ++i) {
+  auto s_products = [&](int t, int g) {   // S(t) += Q K^T over panel group g (0: i = 0..4, 1: i = 5..8)
+    if (!c.wait(KF + g, t & 1)) return false;
+    tc_fence_after();
+    for (int i = g == 0 ? 0 : 5; i < (g == 0 ? 5 : NP); ++i) {
       const int pnl = panel_order(i, h);
-      if (!c.wait(KF + pnl, t & 1)) return false;
-      tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         const uint64_t qo = (uint64_t)((pnl * Q_PANEL + kk * 32) >> 4);
         const uint64_t ko = (uint64_t)((pnl * K_PANEL + kk * 32) >> 4);
         mma_ss(tmem + TM_S(t & 1), q_desc + qo, k_desc + ko, IDESC_QK, (i > 0 || kk > 0) ? 1u : 0u);
       }
-      if (i < 5) tc_commit(c.bar(KE + pnl));   // panels outside the value half: free after S
     }
+    if (g == 0) tc_commit(c.bar(KE + 0));   // the panels outside the value half: free after S
     return true;
   };
   for (int t = 0; t <= n && ok; ++t) {
     if (t < n) {
       // S(t) overwrites the buffer that held P(t - 2): P(t - 2) V must be done.
       if (t >= 2 && !c.wait(SE + (t & 1), ((t - 2) >> 1) & 1)) { ok = false; break; }
-      if (!s_products(t, 0, 5)) { ok = false; break; }
+      if (!s_products(t, 0)) { ok = false; break; }
     }
     if (t >= 1) {
       const int v = t - 1, pb = v & 1;
@@ -215,12 +232,12 @@ __device__ void run_mma(const ACtx& c, const AbsorbedParams& p, const AbsUnit& u
       for (int kk = 0; kk < AN / 16; ++kk)
         mma_ts(tmem + TM_O, tmem + TM_S(pb) + kk * 8, v_desc + (uint64_t)(kk * 16 * 128 >> 4), IDESC_PV,
                (v > 0 || kk > 0) ? 1u : 0u);
-      for (int i = 5; i < NP; ++i) tc_commit(c.bar(KE + panel_order(i, h)));   // value panels free
+      tc_commit(c.bar(KE + 1));   // the value panels: free after P V
       tc_commit(c.bar(SE + pb));
       tc_commit(c.bar(OD + pb));
     }
     if (t < n) {
-      if (!s_products(t, 5, NP)) { ok = false; break; }
+      if (!s_products(t, 1)) { ok = false; break; }
       tc_commit(c.bar(SF + (t & 1)));
     }
   }
@@ -371,7 +388,8 @@ __device__ void run_softmax(const ACtx& c, const AbsorbedParams& p, const AbsUni
 
 __global__ void __launch_bounds__(NTHREADS, 1)
 absorbed_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_c,
-                const __grid_constant__ CUtensorMap tm_b, const AbsorbedParams p) {
+                const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_4,
+                const AbsorbedParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -389,6 +407,7 @@ absorbed_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_c);
     if (p.piece_rows > 0) tma_prefetch_desc(&tm_b);
+    if (p.grouped) tma_prefetch_desc(&tm_4);
   }
   if (warp == 2) {
     tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
@@ -399,9 +418,9 @@ absorbed_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   if (warp == 0) {
-    if (u.ntiles > 0) run_producer(c, p, u, &tm_q, &tm_c, &tm_b, 0, 5);
+    if (u.ntiles > 0) run_producer(c, p, u, &tm_q, &tm_c, &tm_b, &tm_4, 0);
   } else if (warp == 3) {
-    if (u.ntiles > 0) run_producer(c, p, u, &tm_q, &tm_c, &tm_b, 5, NP);
+    if (u.ntiles > 0) run_producer(c, p, u, &tm_q, &tm_c, &tm_b, &tm_4, 1);
   } else if (warp == 1) {
     if (lane == 0) run_mma(c, p, u, tmem);
   } else if (warp >= 4) {
@@ -419,12 +438,12 @@ absorbed_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 }  // namespace
 
 cudaError_t launch_absorbed(const CUtensorMap& tq, const CUtensorMap& tc, const CUtensorMap& tb,
-                            const AbsorbedParams& p, int num_units, cudaStream_t stream) {
+                            const CUtensorMap& t4, const AbsorbedParams& p, int num_units, cudaStream_t stream) {
   static PerDeviceOnce configured;
   const cudaError_t e = configured.run(
       [] { return cudaFuncSetAttribute(absorbed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM); });
   if (e != cudaSuccess) return e;
-  absorbed_kernel<<<num_units, NTHREADS, SMEM, stream>>>(tq, tc, tb, p);
+  absorbed_kernel<<<num_units, NTHREADS, SMEM, stream>>>(tq, tc, tb, t4, p);
   return cudaGetLastError();
 }
 

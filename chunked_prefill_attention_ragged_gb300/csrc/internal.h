@@ -97,6 +97,7 @@ struct AbsorbedParams {
   int64_t num_blocks;
   int32_t oob_row;              // a row coordinate past the cache: the copy fills it with zeros
   int piece_rows;               // rows of one tile load of the block map (0: gather4 only)
+  int grouped;                  // 64-row pieces by runs of panels (the three-dimensional map)
   __nv_bfloat16* o;             // [total_q, H, 512]
   float* lse;                   // [total_q, H] or null
   int* status;
@@ -107,9 +108,11 @@ struct AbsorbedParams {
 
 // The absorbed prefill kernel, one CTA per unit.  tq: q_abs as [total_q * H, 576] rows, box
 // {64, 128}; tc: the cache as [num_blocks * block_size, 576] rows, box {64, 1} (gather4);
-// tb: the same rows with box {64, piece_rows} (any valid map when piece_rows is 0).
+// tb: the same rows with box {64, piece_rows} (any valid map when piece_rows is 0); t4: the
+// rows as {64 columns, rows, 9 column groups} (strides 1152 and 128 bytes), box {64, 64, 4}
+// (any valid map when grouped is 0).
 cudaError_t launch_absorbed(const CUtensorMap& tq, const CUtensorMap& tc, const CUtensorMap& tb,
-                            const AbsorbedParams& p, int num_units, cudaStream_t stream);
+                            const CUtensorMap& t4, const AbsorbedParams& p, int num_units, cudaStream_t stream);
 
 // MLA_PLAN_CTA_PAIRS: 1 when "1" (plan prefills on CTA pairs), 0 when "0", -1 otherwise.
 int cta_pair_mode();

@@ -388,6 +388,17 @@ int mla_absorbed_run(mla_plan_t p, const void* q_abs, const void* cache, int64_t
     const uint32_t box[2] = {64, (uint32_t)piece_rows};
     if (make_tensor_map_bf16(&tb, cache, 2, dims, strides, box) != MLA_OK) return MLA_ERR_CUDA;
   }
+  // 64-row pieces of several adjacent 64-column panels in one copy: the rows seen as
+  // {64 columns, rows, 9 groups of 64 columns}.  Without such a map, one copy per panel.
+  CUtensorMap t4 = tc;
+  int grouped = 0;
+  if (any_keys && piece_rows == 64) {
+    const uint64_t dims[3] = {64, (uint64_t)num_blocks * (uint64_t)bs, 9};
+    const uint64_t strides[2] = {576 * 2, 64 * 2};
+    const uint32_t box[3] = {64, 64, 4};
+    grouped = make_tensor_map_bf16(&t4, cache, 3, dims, strides, box) == MLA_OK ? 1 : 0;
+    if (!grouped) t4 = tc;
+  }
   AbsorbedParams prm;
   prm.units = reinterpret_cast<const AbsUnit*>(p->d_units);
   prm.block_table = block_table;
@@ -396,6 +407,7 @@ int mla_absorbed_run(mla_plan_t p, const void* q_abs, const void* cache, int64_t
   prm.num_blocks = any_keys ? num_blocks : 0;
   prm.oob_row = any_keys ? (int32_t)(num_blocks * p->block_size) : 1;
   prm.piece_rows = any_keys ? piece_rows : 0;
+  prm.grouped = grouped;
   prm.o = static_cast<__nv_bfloat16*>(o_lat);
   prm.lse = lse;
   prm.status = p->d_status;
@@ -409,7 +421,7 @@ int mla_absorbed_run(mla_plan_t p, const void* q_abs, const void* cache, int64_t
   prm.force_timeout = p->forced_timeout_ns != 0;
   prm.wait_limit_ns = prm.force_timeout ? p->forced_timeout_ns : kWaitLimitNs;
   const cudaStream_t s = as_stream(stream);
-  if (launch_absorbed(tq, tc, tb, prm, (int)p->aunits.size(), s) != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_absorbed(tq, tc, tb, t4, prm, (int)p->aunits.size(), s) != cudaSuccess) return MLA_ERR_CUDA;
   if (!stream_capturing(s) && cudaEventRecord(p->last_use, s) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
 }
