@@ -219,11 +219,6 @@ __device__ void run_mma(const ACtx& c, const AbsorbedParams& p, const AbsUnit& u
     return true;
   };
   for (int t = 0; t <= n && ok; ++t) {
-    if (t < n) {
-      // S(t) overwrites the buffer that held P(t - 2): P(t - 2) V must be done.
-      if (t >= 2 && !c.wait(SE + (t & 1), ((t - 2) >> 1) & 1)) { ok = false; break; }
-      if (!s_products(t, 0)) { ok = false; break; }
-    }
     if (t >= 1) {
       const int v = t - 1, pb = v & 1;
       if (!c.wait(PR + pb, (v >> 1) & 1)) { ok = false; break; }
@@ -237,6 +232,9 @@ __device__ void run_mma(const ACtx& c, const AbsorbedParams& p, const AbsUnit& u
       tc_commit(c.bar(OD + pb));
     }
     if (t < n) {
+      // S(t) overwrites the buffer that held P(t - 2): P(t - 2) V must be done.
+      if (t >= 2 && !c.wait(SE + (t & 1), ((t - 2) >> 1) & 1)) { ok = false; break; }
+      if (!s_products(t, 0)) { ok = false; break; }
       if (!s_products(t, 1)) { ok = false; break; }
       tc_commit(c.bar(SF + (t & 1)));
     }
