@@ -17,10 +17,10 @@
 // computed once per half.  Shared memory holds the unit's Q tile (128 x 576 bf16, nine
 // 64-column panels, 144 KB) and one 64-key tile of cache rows in nine 8 KB panel slots
 // (72 KB); V is the tile's own first 512 columns, so the four panels of this CTA's value
-// half serve S = Q K^T and then P V.  Per tile t the S issuer runs the S products over the
-// five panels outside the value half (their slots refill for tile t + 1 at once), then
-// P(t - 1) V(t - 1) (which frees the value panels for tile t's loads), then the S
-// products over the value panels.
+// half serve S = Q K^T and then P V.  Per tile t the MMA issuer runs P(t - 1) V(t - 1)
+// first (which frees the value panels for tile t's loads, so they travel while the next
+// products run), then S(t)'s products over the five panels outside the value half (loaded
+// long before; their slots refill for tile t + 1 at once), then over the value panels.
 //   warps 0, 3 producers (warp 0: the Q tile and the five panels outside the value half,
 //              warp 3: the four value panels): the Q tile with tile loads; cache rows with
 //              one tile load per panel and block piece when the block size lines up with
