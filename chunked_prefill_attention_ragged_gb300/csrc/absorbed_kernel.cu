@@ -22,10 +22,10 @@
 // products run), then S(t)'s products over the five panels outside the value half (loaded
 // long before; their slots refill for tile t + 1 at once), then over the value panels.
 //   warps 0, 3 producers (warp 0: the Q tile and the five panels outside the value half,
-//              warp 3: the four value panels): the Q tile with tile loads; cache rows with
-//              one tile load per panel and block piece when the block size lines up with
-//              the tile (a multiple of 64, or 8..32 dividing 64) and the tile lies inside
-//              kv_len; otherwise (a request's last tile, other block sizes) with
+//              warp 3: the four value panels), each panel group behind one barrier.  A
+//              tile inside kv_len comes by tile copies: one per run of adjacent panels
+//              when the block size is a multiple of 64, one per panel and block when it
+//              is 8, 16 or 32; otherwise (a request's last tile, other block sizes) by
 //              tile::gather4 copies, lanes 0-15 fetching keys 4l .. 4l+3 by slot (rows
 //              past kv_len or in an unknown block read as zeros)
 //   warp 1     MMA issuer (one thread): S = Q K^T (M 128, N 64) into S[t % 2];
