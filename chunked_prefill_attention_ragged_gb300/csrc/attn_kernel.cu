@@ -11,7 +11,8 @@
 // one head run by the two CTAs of a cluster (kPair): each CTA owns 128 of the rows, and
 // the pair's tensor-core products (tcgen05 cta_group::2, M = 256) read each K and V tile
 // half from either CTA, so every CTA loads half of the K/V bytes and its rings hold four
-// stages instead of two.
+// stages instead of two.  Plans use the pair instances only when asked to: on every
+// batch shape measured they ran 3-10% slower than single CTAs.
 //   warps 0, 2  TMA producers: warp 0 loads the Q tile once per unit and K tiles of 128
 //               keys (a CTA of a pair: its 64 of them), warp 2 V tiles (a CTA of a pair:
 //               its 64 of the 128 value columns).
