@@ -77,8 +77,7 @@ enum Bar {
   OD = SE + NSB,        // [tile parity] O += P V done
   FINQ = OD + 2,        // all MMAs of the S issuer drained before TMEM is released
   FINP,                 // the same for the P V issuer
-  XM,                   // [tile parity] softmax half-row max exchange (two barriers)
-  PR = XM + 2,          // [S buffer] P written by every softmax warp (of both CTAs of a pair)
+  PR,                   // [S buffer] P written by every softmax warp (of both CTAs of a pair)
   LR = PR + NSB,        // [unit parity] row sums and max of a unit published
   LFR = LR + 2,         // [unit parity] the epilogue has read them
   OFR = LFR + 2,        // the epilogue (of both CTAs of a pair) has read O: the next
@@ -92,12 +91,15 @@ enum Bar {
 // (which waits for a unit's last two products) both meet that: products complete in
 // order, P(g - 3) V has completed whenever S(g) exists, and P(g + 1) V needs a P (or the
 // epilogue's release of O) not yet given.
-// Exchange area: row max per (tile parity, half) and, per unit parity, both halves'
-// row sums and the row max, 10 x 128 floats.
+// Exchange area: per (tile parity, half, row) an 8-byte word (half-row max, tile) for the
+// max exchange between the two halves of a row, then per unit parity both halves' row
+// sums and the row max: 4096 + 3 x 2 x 128 x 4 bytes.
+constexpr int XCHG_WORDS = 2 * 2 * 128;   // (max, tile) words
+constexpr int XCHG_BYTES = XCHG_WORDS * 8 + 6 * 128 * 4;
 template <bool kPair>
 struct Off {
   static constexpr int XCHG = Lay<kPair>::OFF_BAR + NBAR * 8;
-  static constexpr int MISC = XCHG + 10 * 128 * 4;
+  static constexpr int MISC = XCHG + XCHG_BYTES;
   static constexpr int SMEM = MISC + 16 + 1024;   // + slack for 1024-byte alignment
 };
 static_assert(Off<false>::SMEM <= 227 * 1024 && Off<true>::SMEM <= 227 * 1024, "shared memory budget");
@@ -388,11 +390,38 @@ __device__ void run_mma_pv(const Ctx<kPair>& c, const PrefillParams& p, uint32_t
 }
 
 // ------------------------------------------------------------------ softmax
+// Publish this half's row max for tile `tile` and read the other half's: one 8-byte
+// shared-memory word per half, polled (a bounded spin, as every wait here) until it names
+// the tile.  Cheaper than a 256-arrival barrier on the softmax's critical path.
+template <bool kPair>
+__device__ __forceinline__ bool exchange_max(const Ctx<kPair>& c, uint32_t mine, uint32_t theirs, float m,
+                                             int tile, float* other) {
+  asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(mine), "r"(__float_as_uint(m)), "r"((uint32_t)tile)
+               : "memory");
+  uint32_t v0, v1;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    asm volatile("ld.volatile.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v0), "=r"(v1) : "r"(theirs) : "memory");
+    if (v1 == (uint32_t)tile) break;
+    if ((it & 63) == 63) {
+      if (*c.abort_flag) return false;
+      if (global_timer_ns() - t0 > c.wait_limit_ns) {
+        *c.abort_flag = 1;
+        atomicOr(c.status, MLA_DEVSTAT_TIMEOUT);
+        return false;
+      }
+    }
+  }
+  *other = __uint_as_float(v0);
+  return true;
+}
+
 // Two threads per query row: warps 4-7 own key columns 0-63 of every tile, warps 8-11
 // columns 64-127 (a warp may only touch TMEM lanes 32*(warp%4)..+31, so both halves cover
 // all 128 rows).  The halves agree on the row max through shared memory once per tile;
 // at the end of a unit each publishes its row sum (and half 0 the row max) for the
-// epilogue warps.  Every exchange sits behind an mbarrier so every wait stays bounded.
+// epilogue warps.  Every exchange sits behind an mbarrier or a bounded spin, so every
+// wait can give up.
 template <bool kMerge, bool kPair>
 __device__ void run_softmax(const Ctx<kPair>& c, const PrefillParams& p, uint32_t tmem, float* xchg,
                             int ubeg, int uend) {
@@ -401,8 +430,8 @@ __device__ void run_softmax(const Ctx<kPair>& c, const PrefillParams& p, uint32_
   const int half = (warp - 4) >> 2;          // 0: key columns 0-63, 1: 64-127
   const int row = quad * 32 + lane;
   const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
-  float* xmax = xchg;                        // [2 parity][2 half][128 rows]
-  float* xlm = xchg + 4 * 128;               // [2 unit parity][sum half 0, sum half 1, max][128 rows]
+  const uint32_t xword = smem_addr(xchg);    // [2 parity][2 half][128 rows] of (max, tile)
+  float* xlm = xchg + 2 * XCHG_WORDS;        // [2 unit parity][sum half 0, sum half 1, max][128 rows]
   int s_g = 0, k = 0;                        // tiles and non-empty units so far
   bool ok = true;
   const float NEG_INF = -__int_as_float(0x7f800000);
@@ -466,10 +495,15 @@ __device__ void run_softmax(const Ctx<kPair>& c, const PrefillParams& p, uint32_
         mx[k] = fmax3(fmax3(sv[8 * k], sv[8 * k + 1], sv[8 * k + 2]), fmax3(sv[8 * k + 3], sv[8 * k + 4], sv[8 * k + 5]),
                       fmaxf(sv[8 * k + 6], sv[8 * k + 7]));
       float m_half = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-      xmax[((sg & 1) * 2 + half) * 128 + row] = m_half;
-      mbar_arrive(c.bar(XM + xb));
-      if (!__all_sync(0xffffffffu, c.wait(XM + xb, (sg >> 1) & 1))) { ok = false; break; }
-      const float m_raw = fmaxf(m_half, xmax[((sg & 1) * 2 + (half ^ 1)) * 128 + row]);
+      // The other half's max: each half stores (max, tile) in one 8-byte word and polls
+      // the other's word until it carries this tile (a word per tile parity, so a half
+      // one tile ahead cannot overwrite what its partner has yet to read).
+      float m_other;
+      if (!__all_sync(0xffffffffu,
+                      exchange_max(c, xword + (uint32_t)((xb * 2 + half) * 128 + row) * 8,
+                                   xword + (uint32_t)((xb * 2 + (half ^ 1)) * 128 + row) * 8, m_half, sg, &m_other)))
+        { ok = false; break; }
+      const float m_raw = fmaxf(m_half, m_other);
       const float mt = m_raw * sc2.x;       // tile max in log2 units (-inf stays -inf)
       float m_new = m_used;
       bool rescale = false;
@@ -632,7 +666,7 @@ __device__ void run_epilogue(const Ctx<kPair>& c, const PrefillParams& p, uint32
   const int quad = warp & 3;
   const int row = quad * 32 + lane;
   const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
-  const float* xlm = xchg + 4 * 128;
+  const float* xlm = xchg + 2 * XCHG_WORDS;
   const float NEG_INF = -__int_as_float(0x7f800000);
   int g = 0, k = 0;   // tiles and non-empty units so far
   for (int ui = ubeg; ui < uend; ++ui) {
@@ -738,7 +772,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   if (threadIdx.x == 0) {
     for (int i = 0; i < NBAR; ++i) mbar_init(c.bar(i), 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(c.bar(XM + i), 256);   // every softmax thread
       mbar_init(c.bar(LR + i), 256);
       mbar_init(c.bar(LFR + i), 128);  // every epilogue thread
     }
@@ -753,6 +786,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     *abort_flag = 0;
     fence_barrier_init();
+  }
+  {   // exchange words: no tile yet
+    uint32_t* words = reinterpret_cast<uint32_t*>(smem + Off<kPair>::XCHG);
+    for (int i = threadIdx.x; i < XCHG_WORDS; i += NTHREADS) words[2 * i + 1] = 0xffffffffu;
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_q);
