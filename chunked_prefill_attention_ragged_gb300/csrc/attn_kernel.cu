@@ -368,7 +368,8 @@ __device__ void run_mma_pv(const Ctx<kPair>& c, const PrefillParams& p, uint32_t
     for (int j = 0; j < n; ++j, ++g) {
       // Tiles are counted alike for S buffers and V stages (both advance once per tile).
       const int b = g % NSB, s = g % L::NV;
-      if (!c.wait_pair(PR + b, (g / NSB) & 1) || !c.wait_pair(VF + s, (g / L::NV) & 1)) { ok = false; break; }
+      // V lands tiles ahead; P is the input that arrives last, so it is waited for last.
+      if (!c.wait_pair(VF + s, (g / L::NV) & 1) || !c.wait_pair(PR + b, (g / NSB) & 1)) { ok = false; break; }
       tc_fence_after();
       const uint64_t vd = v_desc0 + (uint64_t)(s * L::V_PANELS * PANEL >> 4);
 #pragma unroll
