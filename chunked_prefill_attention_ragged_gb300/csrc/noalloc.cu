@@ -11,8 +11,8 @@
 //
 // The scratch array (g_noalloc_scratch) is part of the module image, so every GPU that
 // loads this library holds it (about 2 MiB) until the process exits.  Its address is
-// looked up once per device, on the first call made with that device current; make that
-// first call before any stream capture.  All calls share the array and it keeps the last
+// looked up once per device (a host-side symbol lookup), on the first call made with that
+// device current.  All calls share the array and it keeps the last
 // call's contents, so calls that overlap on the GPU (different streams, or several host
 // threads) race on it and must be ordered by the caller.
 #include <cmath>

@@ -403,7 +403,7 @@ MLA_API int mla_merge_state(const void* o_a, const float* lse_a, const void* o_b
  * at most 65536 work units, i.e. sum over requests of ceil(Lq / 128) times
  * num_heads; larger problems return MLA_ERR_UNSUPPORTED before any device
  * work.  The first call on a device looks the array's address up (once per
- * device); make it before any stream capture.  Every call reuses the same
+ * device).  Every call reuses the same
  * array, so calls that overlap on the GPU (other streams, other host
  * threads) race and must be serialised by the caller.  Planning happens on
  * the host at every call.
