@@ -105,6 +105,31 @@ def test_absorbed_prefix_sampled():
     check_attention(f64_of_bf16(o[idx]), lse[idx].double().cpu().numpy(), o_ref, lse_ref, "absorbed prefix")
 
 
+def test_absorbed_bench_shape_sampled():
+    """The benchmarked shape, planned and launched as the benchmark does (4 requests of 2048
+    new rows, each the last of 10240 cache positions, 128 heads, 64-slot blocks out of 1024):
+    per request the first 2 and last 2 rows, every 64-row tile boundary +-1 and 32 seeded
+    random rows, on four heads."""
+    b = wl.random_absorbed(1200, [2048] * 4, [10240] * 4, 128, block_size=64, num_blocks=1024)
+    _, _, o, lse = run_gpu(b)
+    kv, cu = kv_of_requests(b)
+    heads = [0, 37, 90, 127]
+    rng = np.random.default_rng(1202)
+    for r in range(b.batch):
+        lq = int(b.q_lens[r])
+        s = {0, 1, lq - 2, lq - 1}
+        for t in range(64, lq, 64):
+            s.update({t - 1, t, t + 1})
+        s.update(int(x) for x in rng.choice(lq, size=32, replace=False))
+        rows = np.array(sorted(s))
+        q = b.q_abs[b.qo_indptr[r]:b.qo_indptr[r + 1]][:, heads]
+        o_ref, lse_ref = absorbed_attention(q, kv[cu[r]:cu[r + 1]], causal=True, sm_scale=b.sm_scale, rows=rows)
+        idx = torch.from_numpy(b.qo_indptr[r] + rows).cuda()
+        hs = torch.tensor(heads).cuda()
+        check_attention(f64_of_bf16(o[idx][:, hs]), lse[idx][:, hs].double().cpu().numpy(), o_ref, lse_ref,
+                        f"absorbed bench shape, request {r}")
+
+
 def test_absorbed_repeat_runs_bitwise_identical():
     b = wl.random_absorbed(534, [130, 7], [300, 7], 16, block_size=32)
     plan, (q, cache, table), o1, l1 = run_gpu(b)
