@@ -880,8 +880,9 @@ def bench_reference(args, world, rank):
 
 
 def kernel_case(name: str, reps: int = 3):
-    """A small case of one kernel, launched `reps` times and nothing else: the command that
-    the ncu captures under profiles/ run (``--kernel-case``)."""
+    """A fixed case of one kernel (small ones for multi-pass captures; ``absorbed_full`` is the
+    absorbed bench row's shape, for one-pass counters), launched `reps` times and nothing
+    else: the command that the ncu captures under profiles/ run (``--kernel-case``)."""
     import torch
     import chunked_prefill_attention_ragged_gb300 as mla
     from chunked_prefill_attention_ragged_gb300.pipeline import ChunkedPrefill
@@ -911,9 +912,10 @@ def kernel_case(name: str, reps: int = 3):
         v = torch.empty(4096, 128, 128, dtype=torch.bfloat16, device=dev)
         for _ in range(reps):
             mla.mla_up_proj_paged(cache, table, cu, st, 4096, w, 128, k, v)
-    elif name == "absorbed":
-        # 1 request of 64 new rows over 2048 cache positions, 128 heads (128 units)
-        b = absorbed_case(True)
+    elif name in ("absorbed", "absorbed_full"):
+        # small: 1 request of 64 new rows over 2048 cache positions, 128 heads (128 units);
+        # full: the absorbed bench row's shape (16384 units), for one-pass traffic counters
+        b = absorbed_case(name == "absorbed")
         plan = mla.mla_absorbed_plan(b.qo_indptr, b.kv_lens, b.num_heads, b.block_size, causal=True,
                                      sm_scale=b.sm_scale)
         q, cache = dev_bf16(b.q_abs), dev_bf16(b.cache)
@@ -948,9 +950,10 @@ def main():
     ap.add_argument("--no-chunked", action="store_true")
     ap.add_argument("--no-workloads", action="store_true", help="skip the rows of the other workloads")
     ap.add_argument("--no-absorbed", action="store_true", help="skip the absorbed-weight prefill row")
-    ap.add_argument("--kernel-case", choices=["fp8_gather", "up_proj_paged", "up_proj_paged_split", "absorbed"],
+    ap.add_argument("--kernel-case", choices=["fp8_gather", "up_proj_paged", "up_proj_paged_split", "absorbed",
+                                              "absorbed_full"],
                     default=None,
-                    help="launch one kernel on a small case and exit (for profiler captures)")
+                    help="launch one kernel on a fixed case and exit (for profiler captures)")
     args = ap.parse_args()
     if args.kernel_case:
         kernel_case(args.kernel_case)
