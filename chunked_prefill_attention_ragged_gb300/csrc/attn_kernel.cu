@@ -77,8 +77,9 @@ enum Bar {
   OD = SE + NSB,        // [tile parity] O += P V done
   FINQ = OD + 2,        // all MMAs of the S issuer drained before TMEM is released
   FINP,                 // the same for the P V issuer
-  PR,                   // [S buffer] P written by every softmax warp (of both CTAs of a pair)
-  LR = PR + NSB,        // [unit parity] row sums and max of a unit published
+  PR,                   // [S buffer][half row] P written by that half's four softmax warps
+                        // (of both CTAs of a pair): keys 0-63 / 64-127 of the tile
+  LR = PR + 2 * NSB,    // [unit parity] row sums and max of a unit published
   LFR = LR + 2,         // [unit parity] the epilogue has read them
   OFR = LFR + 2,        // the epilogue (of both CTAs of a pair) has read O: the next
                         // unit's first P V may overwrite it
@@ -368,12 +369,17 @@ __device__ void run_mma_pv(const Ctx<kPair>& c, const PrefillParams& p, uint32_t
     for (int j = 0; j < n; ++j, ++g) {
       // Tiles are counted alike for S buffers and V stages (both advance once per tile).
       const int b = g % NSB, s = g % L::NV;
-      // V lands tiles ahead; P is the input that arrives last, so it is waited for last.
-      if (!c.wait_pair(VF + s, (g / L::NV) & 1) || !c.wait_pair(PR + b, (g / NSB) & 1)) { ok = false; break; }
-      tc_fence_after();
+      // V lands tiles ahead; P is the input that arrives last, so it is waited for last,
+      // one half row at a time: keys 0-63 (P columns 0-31) as soon as that half's softmax
+      // warps have written them, keys 64-127 after the other half's.
+      if (!c.wait_pair(VF + s, (g / L::NV) & 1)) { ok = false; break; }
       const uint64_t vd = v_desc0 + (uint64_t)(s * L::V_PANELS * PANEL >> 4);
 #pragma unroll
       for (int kk = 0; kk < BN / 16; ++kk) {
+        if (kk % (BN / 32) == 0) {
+          if (!c.wait_pair(PR + 2 * b + kk / (BN / 32), (g / NSB) & 1)) { ok = false; break; }
+          tc_fence_after();
+        }
         if constexpr (kPair)
           mma_ts_pair(tmem + TM_O, tmem + TM_S(b) + kk * 8, vd + (uint64_t)(kk * 16 * 128 >> 4), Idesc<kPair>::PV,
                       (j > 0 || kk > 0) ? 1u : 0u);
@@ -381,6 +387,7 @@ __device__ void run_mma_pv(const Ctx<kPair>& c, const PrefillParams& p, uint32_t
           mma_ts(tmem + TM_O, tmem + TM_S(b) + kk * 8, vd + (uint64_t)(kk * 16 * 128 >> 4), Idesc<kPair>::PV,
                  (j > 0 || kk > 0) ? 1u : 0u);
       }
+      if (!ok) break;
       c.commit_both(VE + s);
       c.commit(SE + b);
       c.commit_both(OD + (g & 1));
@@ -557,7 +564,7 @@ __device__ void run_softmax(const Ctx<kPair>& c, const PrefillParams& p, uint32_
       m_used = m_new;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) c.arrive_leader(PR + b);
+      if (lane == 0) c.arrive_leader(PR + 2 * b + half);
     }
     if (!ok) break;
     // Hand the unit to the epilogue warps: this half's row sum and the row max.  The
@@ -778,7 +785,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     // One arrival per softmax warp / epilogue warp, of both CTAs in a pair's even CTA.
     const int both = kPair && rank == 0 ? 2 : 1;
-    for (int i = 0; i < NSB; ++i) mbar_init(c.bar(PR + i), 8 * both);
+    for (int i = 0; i < 2 * NSB; ++i) mbar_init(c.bar(PR + i), 4 * both);
     mbar_init(c.bar(OFR), 4 * both);
     if (kPair && rank == 0) {   // own load (with its bytes) + the odd CTA's forwarded arrival
       mbar_init(c.bar(QF), 2);
